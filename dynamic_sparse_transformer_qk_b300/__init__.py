@@ -1,0 +1,276 @@
+"""Condensate-set ("topological") attention on one B300: Python binding.
+
+A thin ctypes layer over ``libtopoattn.so`` (C ABI in ``include/topo_attn.h``).
+It only marshals arguments: shapes are read off torch tensors, outputs and
+the workspace are allocated with torch on the tensors' device, and the current
+torch stream is passed down.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback.  If the library
+is missing, every call raises.
+
+Method ("The Condensate Theorem: Transformers are O(n), Not O(n^2)",
+gist.science explainers of arXiv 2602.06317, technical summary sections 2-3):
+for query position p the condensate set is {0} + {max(0, p-W+1)..p} + the top-k
+of the positions 1..p-W by q . k (float32 score, ties to the lower position);
+the output is the softmax-weighted sum of V over that set.
+
+Layouts: q [B, Hq, nq, d]; k, v [B, Hkv, kv_stride, d] (float32 or bfloat16,
+contiguous, on CUDA); query row r sits at position n - nq + r.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = ["forward", "score_select", "sparse_softmax_pv", "dense_forward", "Workspace",
+           "TopoError", "library_path", "load_library", "workspace_size", "dense_workspace_size",
+           "device_status", "EXPORTS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "libtopoattn.so")
+_lock = threading.Lock()
+_lib = None
+
+# every entry point the header declares
+EXPORTS = ("topo_attn_workspace_size", "dense_attn_workspace_size", "topo_attn_workspace_init",
+           "topo_attn_forward", "topo_attn_score_select", "topo_attn_sparse_softmax_pv",
+           "dense_attn_forward", "topo_attn_strerror", "topo_attn_device_status")
+
+TOPO_OK = 0
+TOPO_KMAX = 256
+
+
+class TopoError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_strerror(status)} (status {status})")
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("n", ctypes.c_int64), ("nq", ctypes.c_int64),
+                ("kv_stride", ctypes.c_int64), ("W", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return _SO
+
+
+def load_library():
+    """Load libtopoattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_SO):
+            raise RuntimeError(f"{_SO} is missing: build it with "
+                               "`python -m dynamic_sparse_transformer_qk_b300.build`")
+        lib = ctypes.CDLL(_SO)
+        P = ctypes.POINTER(Params)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        sig = {
+            "topo_attn_workspace_size": (sz, [P]),
+            "dense_attn_workspace_size": (sz, [P]),
+            "topo_attn_workspace_init": (i, [vp, sz, vp]),
+            "topo_attn_forward": (i, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "topo_attn_score_select": (i, [P, vp, vp, vp, vp, sz, vp]),
+            "topo_attn_sparse_softmax_pv": (i, [P, vp, vp, vp, vp, vp, vp]),
+            "dense_attn_forward": (i, [P, vp, vp, vp, vp, vp, sz, vp]),
+            "topo_attn_strerror": (ctypes.c_char_p, [i]),
+            "topo_attn_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _strerror(status: int) -> str:
+    try:
+        return load_library().topo_attn_strerror(status).decode()
+    except Exception:  # library not loadable: still say something
+        return "status"
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def make_params(q: torch.Tensor, k: torch.Tensor, *, W: int, topk: int, n: int | None = None,
+                scale: float | None = None) -> Params:
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, Hq, nq, d] and k [B, Hkv, kv_stride, d]")
+    B, Hq, nq, d = q.shape
+    Bk, Hkv, stride, dk = k.shape
+    if Bk != B or dk != d:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} vs k {tuple(k.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return Params(B, Hq, Hkv, d, stride if n is None else n, nq, stride, W, topk, scale,
+                  _dtype_code(q))
+
+
+def _check(*ts: torch.Tensor):
+    dev = ts[0].device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for t in ts:
+        if t.device != dev or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous and on one device")
+        if t.dtype != ts[0].dtype:
+            raise ValueError("q, k, v must share one dtype")
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def workspace_size(p: Params) -> int:
+    return int(load_library().topo_attn_workspace_size(ctypes.byref(p)))
+
+
+def dense_workspace_size(p: Params) -> int:
+    return int(load_library().dense_attn_workspace_size(ctypes.byref(p)))
+
+
+class Workspace:
+    """A zero-initialised device buffer the library may use for scratch.
+
+    The library leaves it zeroed after every completed call, so one Workspace
+    can serve any number of stream-ordered calls."""
+
+    def __init__(self, device=None, nbytes: int = 0):
+        self.device = torch.device(device or "cuda")
+        self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+
+    def ensure(self, nbytes: int) -> "Workspace":
+        if self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+
+_default_ws: dict = {}
+
+
+def _workspace(ws: Workspace | None, device, nbytes: int, stream) -> Workspace:
+    if ws is None:
+        key = (device, _stream(stream))
+        ws = _default_ws.get(key)
+        if ws is None:
+            ws = _default_ws[key] = Workspace(device, nbytes)
+    return ws.ensure(nbytes)
+
+
+def _raise(rc: int, what: str):
+    if rc != TOPO_OK:
+        raise TopoError(rc, what)
+
+
+def forward(q, k, v, *, W: int, topk: int, n: int | None = None, scale: float | None = None,
+            want_idx: bool = False, want_excl: bool = False, out=None, idx=None, excl=None,
+            workspace: Workspace | None = None, stream=None):
+    """Condensate-set attention.  Returns (out, idx or None, excl or None)."""
+    _check(q, k, v)
+    lib = load_library()
+    p = make_params(q, k, W=W, topk=topk, n=n, scale=scale)
+    B, Hq, nq, d = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q.device)
+    if want_idx and idx is None:
+        idx = torch.empty((B, Hq, nq, 1 + W + topk), dtype=torch.int32, device=q.device)
+    if want_excl and excl is None:
+        excl = torch.empty((B, Hq, nq), dtype=torch.float32, device=q.device)
+    need = workspace_size(p)
+    if need == 0:
+        _raise(-1 if p.d in (64, 128) else -2, "topo_attn_workspace_size")
+    ws = _workspace(workspace, q.device, need, stream)
+    rc = lib.topo_attn_forward(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               out.data_ptr(), idx.data_ptr() if idx is not None else None,
+                               excl.data_ptr() if excl is not None else None, ws.ptr, ws.nbytes,
+                               _stream(stream))
+    _raise(rc, "topo_attn_forward")
+    return out, idx, excl
+
+
+def score_select(q, k, *, W: int, topk: int, n: int | None = None, scale: float | None = None,
+                 idx=None, workspace: Workspace | None = None, stream=None):
+    """The condensate sets alone: int32 [B, Hq, nq, 1+W+k], ascending, -1 padded."""
+    _check(q, k)
+    lib = load_library()
+    p = make_params(q, k, W=W, topk=topk, n=n, scale=scale)
+    B, Hq, nq, _ = q.shape
+    if idx is None:
+        idx = torch.empty((B, Hq, nq, 1 + W + topk), dtype=torch.int32, device=q.device)
+    need = workspace_size(p)
+    if need == 0:
+        _raise(-1 if p.d in (64, 128) else -2, "topo_attn_workspace_size")
+    ws = _workspace(workspace, q.device, need, stream)
+    rc = lib.topo_attn_score_select(ctypes.byref(p), q.data_ptr(), k.data_ptr(), idx.data_ptr(),
+                                    ws.ptr, ws.nbytes, _stream(stream))
+    _raise(rc, "topo_attn_score_select")
+    return idx
+
+
+def sparse_softmax_pv(q, k, v, idx, *, W: int, topk: int, n: int | None = None,
+                      scale: float | None = None, out=None, stream=None):
+    """Softmax over given index rows idx [B, Hq, nq, 1+W+k] and the weighted sum of V."""
+    _check(q, k, v)
+    lib = load_library()
+    p = make_params(q, k, W=W, topk=topk, n=n, scale=scale)
+    B, Hq, nq, d = q.shape
+    if idx.dtype != torch.int32 or tuple(idx.shape) != (B, Hq, nq, 1 + W + topk) \
+            or not idx.is_contiguous() or idx.device != q.device:
+        raise ValueError("idx must be contiguous int32 [B, Hq, nq, 1+W+k] on q's device")
+    if out is None:
+        out = torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q.device)
+    rc = lib.topo_attn_sparse_softmax_pv(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
+                                         v.data_ptr(), idx.data_ptr(), out.data_ptr(),
+                                         _stream(stream))
+    _raise(rc, "topo_attn_sparse_softmax_pv")
+    return out
+
+
+def dense_forward(q, k, v, *, n: int | None = None, scale: float | None = None, out=None,
+                  workspace: Workspace | None = None, stream=None):
+    """Dense causal attention over keys 0..p (the full-attention layer)."""
+    _check(q, k, v)
+    lib = load_library()
+    p = make_params(q, k, W=1, topk=0, n=n, scale=scale)
+    B, Hq, nq, d = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q.device)
+    need = dense_workspace_size(p)
+    if need == 0:
+        _raise(-1 if p.d in (64, 128) else -2, "dense_attn_workspace_size")
+    ws = _workspace(workspace, q.device, need, stream)
+    rc = lib.dense_attn_forward(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                out.data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
+    _raise(rc, "dense_attn_forward")
+    return out
+
+
+def device_status(ws: Workspace, stream=None) -> int:
+    """Read and clear the workspace's device status word (synchronises)."""
+    st = ctypes.c_int(0)
+    rc = load_library().topo_attn_device_status(ws.ptr, ctypes.byref(st), _stream(stream))
+    _raise(rc, "topo_attn_device_status")
+    return st.value

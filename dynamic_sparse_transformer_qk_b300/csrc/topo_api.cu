@@ -1,0 +1,384 @@
+// topo_api.cu -- the C ABI of libtopoattn.so (declared in include/topo_attn.h):
+// argument checks, launch planning, workspace layout, TMA descriptors and
+// kernel dispatch.  No allocation, no synchronisation (except the explicit
+// status read-back), no global mutable state beyond lazily resolved driver
+// entry points and per-kernel attribute set-up.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "topo_attn.h"
+#include "topo_launch.cuh"
+
+namespace {
+
+using topo::Geom;
+using topo::kTile;
+
+constexpr long long kMaxRows = (1LL << 31) - 2 * kTile;  // TMA row coordinate is int32
+
+struct Plan {
+  bool bf16 = false;
+  int D = 0, NC = 1, KE = 1, KP = 32;
+  long long ncols = 0, ncb = 0, units = 0;
+  // select (or dense) pass
+  long long L = kTile;
+  int nsplit = 1, stages = 2, smem = 0;
+  // excluded-mass pass
+  long long Le = kTile;
+  int nsplit_e = 1, stages_e = 2, smem_e = 0;
+  // workspace layout (bytes)
+  size_t off_cnt = 0, off_cnt_e = 0, off_lists = 0, off_thr = 0, off_part = 0, total = 0;
+};
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline int pow2_at_least(long long x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+int check_params(const topo_attn_params* p) {
+  if (!p) return TOPO_ERR_INVALID_ARG;
+  if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0) return TOPO_ERR_INVALID_ARG;
+  if (p->B > 65535 || p->Hkv > 65535) return TOPO_ERR_INVALID_ARG;
+  if (p->n < 1 || p->nq < 1 || p->nq > p->n || p->kv_stride < p->n) return TOPO_ERR_INVALID_ARG;
+  if (p->n > (1LL << 31) - 1) return TOPO_ERR_INVALID_ARG;
+  if (p->W < 1 || p->k < 0) return TOPO_ERR_INVALID_ARG;
+  if (!isfinite(p->scale)) return TOPO_ERR_INVALID_ARG;
+  if (p->dtype != TOPO_F32 && p->dtype != TOPO_BF16) return TOPO_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 128) return TOPO_ERR_UNSUPPORTED;
+  if (p->k > TOPO_KMAX) return TOPO_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->Hkv * p->kv_stride > kMaxRows) return TOPO_ERR_UNSUPPORTED;
+  return TOPO_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+// Keys per split: enough CTAs to fill every SM, chosen so that the last wave
+// is as full as possible (all splits of a pass take about the same time).
+long long choose_split(long long units, long long nkeys, int slots) {
+  if (nkeys <= kTile) return kTile;
+  const long long smax = nkeys / (4 * kTile) > 1 ? nkeys / (4 * kTile) : 1;
+  double best = -1.0;
+  long long best_s = 1;
+  for (long long s = 1; s <= smax && s <= 4096; ++s) {
+    const long long total = units * s;
+    const long long waves = ceil_div(total, slots);
+    const double eff = (double)total / (double)(waves * slots);
+    if (eff > best + 1e-9) {
+      best = eff;
+      best_s = s;
+    }
+    if (total >= 8LL * slots) break;
+  }
+  return ceil_div(ceil_div(nkeys, best_s), kTile) * kTile;
+}
+
+int stages_for(int stage_bytes, int fixed_bytes, int min_ring) {
+  int st = (topo::kMaxSmem - fixed_bytes) / stage_bytes;
+  if (st > 16) st = 16;
+  while (st > 2 && st * stage_bytes > topo::kMaxSmem - fixed_bytes) --st;
+  if (st * stage_bytes < min_ring) st = (min_ring + stage_bytes - 1) / stage_bytes;
+  return st;
+}
+
+// Plan for the condensate-set passes (dense=false) or the dense pass.
+int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
+  int rc = check_params(p);
+  if (rc != TOPO_OK) return rc;
+  P->bf16 = p->dtype == TOPO_BF16;
+  P->D = p->d;
+  const int g = p->Hq / p->Hkv;
+  P->ncols = p->nq * g;
+  P->NC = pow2_at_least(P->ncols) < 8 ? pow2_at_least(P->ncols) : 8;
+  P->ncb = ceil_div(P->ncols, P->NC);
+  P->units = (long long)p->B * p->Hkv * P->ncb;
+  P->KP = pow2_at_least(p->k > 32 ? p->k : 32);
+  P->KE = P->KP / 32;
+  const int es = P->bf16 ? 2 : 4;
+  const int tileb = kTile * P->D * es;
+  const int slots = sm_count();
+  const long long pos_max = p->n - 1;
+  if (!dense) {
+    const long long ncand = p->k > 0 ? pos_max - p->W : 0;
+    P->L = choose_split(P->units, ncand > 0 ? ncand : 0, slots);
+    P->nsplit = ncand > 0 ? (int)ceil_div(ncand, P->L) : 1;
+    const int cap = topo::cap_for(P->KE);
+    const topo::Smem base(0, 0, P->D, P->NC, topo::kConsumerWarps * P->NC * cap * 8);
+    const int tail = P->NC * P->KP * 8 > P->NC * P->KP * 4 + topo::kWarps * 2048
+                         ? P->NC * P->KP * 8
+                         : P->NC * P->KP * 4 + topo::kWarps * 2048;
+    P->stages = stages_for(tileb + 16, base.total, tail > 32768 ? tail : 32768);
+    P->smem = topo::Smem(tileb, P->stages, P->D, P->NC, topo::kConsumerWarps * P->NC * cap * 8).total;
+    // excluded-mass pass: keys 0..p
+    P->Le = choose_split(P->units, pos_max + 1, slots);
+    P->nsplit_e = (int)ceil_div(pos_max + 1, P->Le);
+    const topo::Smem base_e(0, 0, P->D, P->NC, topo::kWarps * P->NC * 16);
+    P->stages_e = stages_for(tileb + 16, base_e.total, 32768);
+    P->smem_e = topo::Smem(tileb, P->stages_e, P->D, P->NC, topo::kWarps * P->NC * 16).total;
+  } else {
+    P->L = choose_split(P->units, pos_max + 1, slots);
+    P->nsplit = (int)ceil_div(pos_max + 1, P->L);
+    const int pbuf = topo::kConsumerWarps * kTile * P->NC * 4;
+    const topo::Smem base(0, 0, P->D, P->NC, pbuf);
+    const int red = topo::kConsumerWarps * P->NC * (P->D + 2) * 4;
+    P->stages = stages_for(2 * tileb + 16, base.total, red > 32768 ? red : 32768);
+    P->smem = topo::Smem(2 * tileb, P->stages, P->D, P->NC, pbuf).total;
+  }
+  if (P->smem > topo::kMaxSmem || P->smem_e > topo::kMaxSmem) return TOPO_ERR_UNSUPPORTED;
+  if (P->ncb * P->nsplit > 0x7fffffffLL || P->ncb * P->nsplit_e > 0x7fffffffLL)
+    return TOPO_ERR_UNSUPPORTED;
+  // workspace: status word, counters, then per-pass buffers
+  size_t o = 256;
+  P->off_cnt = o;
+  o = align256(o + (size_t)P->units * 4);
+  P->off_cnt_e = o;
+  o = align256(o + (size_t)P->units * 4);
+  if (!dense) {
+    P->off_lists = o;
+    o = align256(o + (size_t)P->units * P->nsplit * P->NC * P->KP * 8);
+    P->off_thr = o;
+    o = align256(o + (size_t)P->units * P->NC * 8);
+    P->off_part = o;
+    o = align256(o + (size_t)P->units * P->nsplit_e * P->NC * 16);
+  } else {
+    P->off_part = o;
+    o = align256(o + (size_t)P->units * P->nsplit * P->NC * (P->D + 2) * 4);
+  }
+  P->total = o;
+  return TOPO_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// 2-D map over the rows of k or v ([B*Hkv*kv_stride, d]); box = 128 bytes of
+// one row x 64 rows, 128-byte swizzle.
+int make_map(CUtensorMap* map, const void* base, const topo_attn_params* p) {
+  auto fn = encode_fn();
+  if (!fn) return TOPO_ERR_CUDA;
+  const bool bf16 = p->dtype == TOPO_BF16;
+  const int es = bf16 ? 2 : 4;
+  const cuuint64_t rows = (cuuint64_t)p->B * p->Hkv * p->kv_stride;
+  const cuuint64_t dims[2] = {(cuuint64_t)p->d, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)p->d * es};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kTile};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TOPO_OK : TOPO_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+Geom base_geom(const topo_attn_params* p, const Plan& P) {
+  Geom G;
+  memset(&G, 0, sizeof G);
+  G.B = p->B;
+  G.Hq = p->Hq;
+  G.Hkv = p->Hkv;
+  G.g = p->Hq / p->Hkv;
+  G.n = p->n;
+  G.nq = p->nq;
+  G.kv_stride = p->kv_stride;
+  G.W = p->W;
+  G.topk = p->k;
+  G.scale = p->scale;
+  G.ncols = P.ncols;
+  G.ncb = P.ncb;
+  return G;
+}
+
+int to_status(cudaError_t e) {
+  if (e == cudaSuccess) return TOPO_OK;
+  return TOPO_ERR_CUDA;
+}
+
+template <class F>
+int dispatch(bool bf16, int D, F&& f) {
+  if (bf16) {
+    if (D == 128) return to_status(f(topo::Launcher<true, 128>()));
+    return to_status(f(topo::Launcher<true, 64>()));
+  }
+  if (D == 128) return to_status(f(topo::Launcher<false, 128>()));
+  return to_status(f(topo::Launcher<false, 64>()));
+}
+
+// The select pass (and, with excl, the excluded-mass pass).
+int run_topo(const topo_attn_params* p, const void* q, const void* k, const void* v, float* out,
+             int32_t* idx, float* excl, void* ws, size_t ws_bytes, cudaStream_t st) {
+  Plan P;
+  int rc = make_plan(p, false, &P);
+  if (rc != TOPO_OK) return rc;
+  if (!q || !k) return TOPO_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || (v && !aligned16(v))) return TOPO_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < P.total)
+    return TOPO_ERR_WORKSPACE;
+  CUtensorMap mk;
+  rc = make_map(&mk, k, p);
+  if (rc != TOPO_OK) return rc;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  Geom G = base_geom(p, P);
+  G.qp = q;
+  G.kp = k;
+  G.vp = v;
+  G.out = out;
+  G.idx = idx;
+  G.excl = excl;
+  G.status = reinterpret_cast<int*>(w);
+  G.counters = reinterpret_cast<int*>(w + P.off_cnt);
+  G.lists = reinterpret_cast<unsigned long long*>(w + P.off_lists);
+  G.thr = reinterpret_cast<unsigned long long*>(w + P.off_thr);
+  G.partials = reinterpret_cast<float*>(w + P.off_part);
+  G.L = P.L;
+  G.nsplit_max = P.nsplit;
+  G.stages = P.stages;
+  G.flags = (out ? topo::kDoPV : 0) | (idx ? topo::kDoIdx : 0) | (excl ? topo::kSaveThr : 0);
+  const dim3 grid((unsigned)(P.ncb * P.nsplit), (unsigned)p->Hkv, (unsigned)p->B);
+  rc = dispatch(P.bf16, P.D, [&](auto L) { return L.select(P.NC, P.KE, mk, G, grid, P.smem, st); });
+  if (rc != TOPO_OK || !excl) return rc;
+  Geom E = G;
+  E.counters = reinterpret_cast<int*>(w + P.off_cnt_e);
+  E.L = P.Le;
+  E.nsplit_max = P.nsplit_e;
+  E.stages = P.stages_e;
+  const dim3 grid_e((unsigned)(P.ncb * P.nsplit_e), (unsigned)p->Hkv, (unsigned)p->B);
+  return dispatch(P.bf16, P.D, [&](auto L) { return L.excl(P.NC, mk, E, grid_e, P.smem_e, st); });
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t topo_attn_workspace_size(const topo_attn_params* p) {
+  Plan P;
+  return make_plan(p, false, &P) == TOPO_OK ? P.total : 0;
+}
+
+size_t dense_attn_workspace_size(const topo_attn_params* p) {
+  Plan P;
+  return make_plan(p, true, &P) == TOPO_OK ? P.total : 0;
+}
+
+int topo_attn_workspace_init(void* ws, size_t bytes, topo_stream_t stream) {
+  if (!ws) return TOPO_ERR_INVALID_ARG;
+  return to_status(cudaMemsetAsync(ws, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int topo_attn_forward(const topo_attn_params* p, const void* q, const void* k, const void* v,
+                      float* out, int32_t* idx, float* excl, void* ws, size_t ws_bytes,
+                      topo_stream_t stream) {
+  if (!out || !v) return TOPO_ERR_INVALID_ARG;
+  return run_topo(p, q, k, v, out, idx, excl, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topo_attn_score_select(const topo_attn_params* p, const void* q, const void* k, int32_t* idx,
+                           void* ws, size_t ws_bytes, topo_stream_t stream) {
+  if (!idx) return TOPO_ERR_INVALID_ARG;
+  return run_topo(p, q, k, nullptr, nullptr, idx, nullptr, ws, ws_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topo_attn_sparse_softmax_pv(const topo_attn_params* p, const void* q, const void* k,
+                                const void* v, const int32_t* idx, float* out,
+                                topo_stream_t stream) {
+  const int rc = check_params(p);
+  if (rc != TOPO_OK) return rc;
+  if (!q || !k || !v || !idx || !out) return TOPO_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return TOPO_ERR_INVALID_ARG;
+  Plan P;
+  P.ncols = p->nq * (p->Hq / p->Hkv);
+  P.ncb = 1;
+  Geom G = base_geom(p, P);
+  G.qp = q;
+  G.kp = k;
+  G.vp = v;
+  G.out = out;
+  G.idx = const_cast<int*>(idx);
+  const long long nrows = (long long)p->B * p->Hq * p->nq;
+  if ((nrows + 3) / 4 > 0x7fffffffLL) return TOPO_ERR_UNSUPPORTED;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return dispatch(p->dtype == TOPO_BF16, p->d, [&](auto L) { return L.pv(G, nrows, st); });
+}
+
+int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, const void* v,
+                       float* out, void* ws, size_t ws_bytes, topo_stream_t stream) {
+  Plan P;
+  int rc = make_plan(p, true, &P);
+  if (rc != TOPO_OK) return rc;
+  if (!q || !k || !v || !out) return TOPO_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return TOPO_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < P.total)
+    return TOPO_ERR_WORKSPACE;
+  CUtensorMap mk, mv;
+  rc = make_map(&mk, k, p);
+  if (rc == TOPO_OK) rc = make_map(&mv, v, p);
+  if (rc != TOPO_OK) return rc;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  Geom G = base_geom(p, P);
+  G.qp = q;
+  G.kp = k;
+  G.vp = v;
+  G.out = out;
+  G.status = reinterpret_cast<int*>(w);
+  G.counters = reinterpret_cast<int*>(w + P.off_cnt);
+  G.partials = reinterpret_cast<float*>(w + P.off_part);
+  G.L = P.L;
+  G.nsplit_max = P.nsplit;
+  G.stages = P.stages;
+  const dim3 grid((unsigned)(P.ncb * P.nsplit), (unsigned)p->Hkv, (unsigned)p->B);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return dispatch(P.bf16, P.D, [&](auto L) { return L.dense(P.NC, mk, mv, G, grid, P.smem, st); });
+}
+
+const char* topo_attn_strerror(int status) {
+  switch (status) {
+    case TOPO_OK: return "ok";
+    case TOPO_ERR_INVALID_ARG: return "invalid argument (shape, pointer or alignment)";
+    case TOPO_ERR_UNSUPPORTED: return "unsupported configuration (d, k, dtype or size)";
+    case TOPO_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case TOPO_ERR_CUDA: return "a CUDA call failed while enqueueing work";
+    case TOPO_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int topo_attn_device_status(void* ws, int* status, topo_stream_t stream) {
+  if (!ws || !status) return TOPO_ERR_INVALID_ARG;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int h = 0;
+  if (cudaMemcpyAsync(&h, ws, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemsetAsync(ws, 0, sizeof h, st) != cudaSuccess)
+    return TOPO_ERR_CUDA;
+  *status = h;
+  return TOPO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// topo_launch.cuh -- typed launchers for the kernels of topo_kernels.cuh.
+// Each (dtype, d) pair is instantiated in its own translation unit.
+#pragma once
+
+#include "topo_kernels.cuh"
+
+namespace topo {
+
+constexpr int kMaxSmem = 232448;  // opt-in shared memory per block on sm_100-class parts
+
+template <auto Kern>
+cudaError_t allow_smem() {
+  static const cudaError_t e =
+      cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  return e;
+}
+
+template <bool BF16, int D>
+struct Launcher {
+  static cudaError_t select(int NC, int KE, const CUtensorMap& mk, const Geom& G, dim3 grid,
+                            int smem, cudaStream_t st);
+  static cudaError_t excl(int NC, const CUtensorMap& mk, const Geom& G, dim3 grid, int smem,
+                          cudaStream_t st);
+  static cudaError_t dense(int NC, const CUtensorMap& mk, const CUtensorMap& mv, const Geom& G,
+                           dim3 grid, int smem, cudaStream_t st);
+  static cudaError_t pv(const Geom& G, long long nrows, cudaStream_t st);
+};
+
+template <bool BF16, int D, int NC, int KE>
+cudaError_t run_select(const CUtensorMap& mk, const Geom& G, dim3 grid, int smem,
+                       cudaStream_t st) {
+  constexpr auto kern = &topo_select_kernel<BF16, D, NC, KE>;
+  const cudaError_t e = allow_smem<kern>();
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(mk, G);
+  return cudaGetLastError();
+}
+
+template <bool BF16, int D, int NC>
+cudaError_t run_select_ke(int KE, const CUtensorMap& mk, const Geom& G, dim3 grid, int smem,
+                          cudaStream_t st) {
+  switch (KE) {
+    case 1: return run_select<BF16, D, NC, 1>(mk, G, grid, smem, st);
+    case 2: return run_select<BF16, D, NC, 2>(mk, G, grid, smem, st);
+    case 4: return run_select<BF16, D, NC, 4>(mk, G, grid, smem, st);
+    case 8: return run_select<BF16, D, NC, 8>(mk, G, grid, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::select(int NC, int KE, const CUtensorMap& mk, const Geom& G,
+                                      dim3 grid, int smem, cudaStream_t st) {
+  switch (NC) {
+    case 1: return run_select_ke<BF16, D, 1>(KE, mk, G, grid, smem, st);
+    case 2: return run_select_ke<BF16, D, 2>(KE, mk, G, grid, smem, st);
+    case 4: return run_select_ke<BF16, D, 4>(KE, mk, G, grid, smem, st);
+    case 8: return run_select_ke<BF16, D, 8>(KE, mk, G, grid, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BF16, int D, int NC>
+cudaError_t run_excl(const CUtensorMap& mk, const Geom& G, dim3 grid, int smem, cudaStream_t st) {
+  constexpr auto kern = &topo_excl_kernel<BF16, D, NC>;
+  const cudaError_t e = allow_smem<kern>();
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(mk, G);
+  return cudaGetLastError();
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::excl(int NC, const CUtensorMap& mk, const Geom& G, dim3 grid,
+                                    int smem, cudaStream_t st) {
+  switch (NC) {
+    case 1: return run_excl<BF16, D, 1>(mk, G, grid, smem, st);
+    case 2: return run_excl<BF16, D, 2>(mk, G, grid, smem, st);
+    case 4: return run_excl<BF16, D, 4>(mk, G, grid, smem, st);
+    case 8: return run_excl<BF16, D, 8>(mk, G, grid, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BF16, int D, int NC>
+cudaError_t run_dense(const CUtensorMap& mk, const CUtensorMap& mv, const Geom& G, dim3 grid,
+                      int smem, cudaStream_t st) {
+  constexpr auto kern = &dense_kernel<BF16, D, NC>;
+  const cudaError_t e = allow_smem<kern>();
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(mk, mv, G);
+  return cudaGetLastError();
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::dense(int NC, const CUtensorMap& mk, const CUtensorMap& mv,
+                                     const Geom& G, dim3 grid, int smem, cudaStream_t st) {
+  switch (NC) {
+    case 1: return run_dense<BF16, D, 1>(mk, mv, G, grid, smem, st);
+    case 2: return run_dense<BF16, D, 2>(mk, mv, G, grid, smem, st);
+    case 4: return run_dense<BF16, D, 4>(mk, mv, G, grid, smem, st);
+    case 8: return run_dense<BF16, D, 8>(mk, mv, G, grid, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::pv(const Geom& G, long long nrows, cudaStream_t st) {
+  const long long blocks = (nrows + 3) / 4;
+  sparse_pv_kernel<BF16, D><<<(unsigned)blocks, 128, 0, st>>>(G);
+  return cudaGetLastError();
+}
+
+extern template struct Launcher<false, 64>;
+extern template struct Launcher<false, 128>;
+extern template struct Launcher<true, 64>;
+extern template struct Launcher<true, 128>;
+
+}  // namespace topo

@@ -1,0 +1,148 @@
+/*
+ * topo_attn.h -- C ABI of libtopoattn.so: condensate-set ("topological")
+ * attention on one NVIDIA B300 (sm_103a).
+ *
+ * Method: "The Condensate Theorem: Transformers are O(n), Not O(n^2)"
+ * (J. L. Ruiz Williams, arXiv 2602.06317), as restated by the gist.science
+ * explainer pages; cited below as [fr S2] = French page, Resume Technique
+ * section 2, [ko S3] = Korean page, technical summary section 3, and so on.
+ *
+ *   [fr S2] / [zh S3]  for each query position i the condensate set is
+ *                      C_i = {anchor 0} U {the W most recent positions}
+ *                            U {the k positions with the largest q_i . k_j}.
+ *   [fr S3]            the softmax is taken over the indices in C_i only.
+ *   [ko S3]            q . K^T scores are recomputed at every step to find C_i
+ *                      (dynamic selection), so every causal key is scored.
+ *   [fr S3] / [ko S2]  the weights left out are claimed to fall below the
+ *                      float32 ULP; the optional `excl` output measures them.
+ *   [zh S3]            "pillar" layers keep full attention: dense_attn_forward.
+ *
+ * Readings fixed by this library where the pages are silent:
+ *   - query row r of a call sits at absolute position p = n - nq + r and sees
+ *     keys 0..p (causal);
+ *   - the window is {max(0, p-W+1) .. p} (it includes p);
+ *   - top-k candidates are 1 .. p-W; with fewer than k candidates all are
+ *     taken;
+ *   - ranking uses the float32 score acc = +0; for c in 0..d-1:
+ *     acc = fma(q[c], k[c], acc) (one rounding per step), ordered by (score
+ *     descending, index ascending): equal scores go to the lower index;
+ *   - query head h reads KV head h / (Hq / Hkv).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing and keeps no global mutable state; it is
+ *     thread-safe.  Work is enqueued on `stream` (a cudaStream_t, 0 = legacy
+ *     default stream) and the call returns without synchronising.
+ *   - Layouts are row-major with d fastest:
+ *       q    [B, Hq,  nq,        d]  dtype
+ *       k, v [B, Hkv, kv_stride, d]  dtype (rows n .. kv_stride-1 are never read)
+ *       out  [B, Hq,  nq,        d]  float32
+ *       idx  [B, Hq,  nq, 1+W+k]     int32, C_i ascending, padded with -1
+ *       excl [B, Hq,  nq]            float32
+ *     q, k, v must be 16-byte aligned.
+ *   - Return value: TOPO_OK or a negative TOPO_ERR_* code.  Argument errors
+ *     are detected on the host before anything is enqueued.  Faults of
+ *     kernels already enqueued surface at the caller's next synchronisation,
+ *     as usual in CUDA.  Inputs are assumed finite; NaN or Inf inputs give
+ *     unspecified (but memory-safe) results.
+ *   - Workspace: `ws` is a caller-owned device buffer of at least
+ *     topo_attn_workspace_size() (resp. dense_attn_workspace_size()) bytes,
+ *     256-byte aligned.  It must be zero-filled once before its first use
+ *     (topo_attn_workspace_init); every call that completes leaves it ready
+ *     for the next one.  Calls sharing one workspace must be ordered on one
+ *     stream.  After a TOPO_ERR_DEVICE_TIMEOUT report, zero it again.
+ */
+#ifndef TOPO_ATTN_H
+#define TOPO_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+typedef struct CUstream_st *topo_stream_t;
+
+#define TOPO_KMAX 256 /* largest supported k */
+
+enum {
+  TOPO_OK = 0,
+  TOPO_ERR_INVALID_ARG = -1,      /* bad shape, null required pointer, misaligned pointer */
+  TOPO_ERR_UNSUPPORTED = -2,      /* d, k or dtype outside the supported set */
+  TOPO_ERR_WORKSPACE = -3,        /* workspace missing, too small or misaligned */
+  TOPO_ERR_CUDA = -4,             /* a CUDA runtime/driver call failed at enqueue time */
+  TOPO_ERR_DEVICE_TIMEOUT = -5    /* a bounded device-side wait gave up (see topo_attn_device_status) */
+};
+
+typedef enum { TOPO_F32 = 0, TOPO_BF16 = 1 } topo_dtype;
+
+typedef struct {
+  int32_t B;          /* sequences, >= 1 */
+  int32_t Hq;         /* query heads, >= 1, multiple of Hkv */
+  int32_t Hkv;        /* key/value heads, >= 1 */
+  int32_t d;          /* head dimension: 64 or 128 */
+  int64_t n;          /* causal length: keys 0..n-1 are valid, >= 1 */
+  int64_t nq;         /* query rows per (sequence, head), 1 <= nq <= n */
+  int64_t kv_stride;  /* rows allocated per (sequence, KV head) in k and v, >= n */
+  int32_t W;          /* window length, >= 1 */
+  int32_t k;          /* top-k, 0 <= k <= TOPO_KMAX */
+  float scale;        /* logit = scale * (q . k_j); finite */
+  int32_t dtype;      /* topo_dtype of q, k, v */
+} topo_attn_params;
+
+/* Workspace bytes needed by topo_attn_forward / topo_attn_score_select for
+ * these parameters; 0 if the parameters are invalid or unsupported. */
+size_t topo_attn_workspace_size(const topo_attn_params *p);
+
+/* Workspace bytes needed by dense_attn_forward; 0 if invalid. */
+size_t dense_attn_workspace_size(const topo_attn_params *p);
+
+/* Zero `bytes` of workspace on `stream` (cudaMemsetAsync). */
+int topo_attn_workspace_init(void *ws, size_t bytes, topo_stream_t stream);
+
+/*
+ * Condensate-set attention [fr S2-S3]: per query row, score every causal key
+ * in float32 (the ranking score above), select C_i, take the softmax over C_i
+ * in float32 and write out = sum_j w_j v_j / sum_j w_j.
+ *   out  : required.
+ *   idx  : optional (NULL to skip): C_i per row.
+ *   excl : optional (NULL to skip): the dense-softmax mass outside C_i,
+ *          sum_{j <= p, j not in C_i} softmax_j(scale * q . k), computed by a
+ *          second pass over K.
+ */
+int topo_attn_forward(const topo_attn_params *p, const void *q, const void *k, const void *v,
+                      float *out, int32_t *idx, float *excl, void *ws, size_t ws_bytes,
+                      topo_stream_t stream);
+
+/* The scoring and selection steps alone [fr S2, ko S3]: writes idx (required). */
+int topo_attn_score_select(const topo_attn_params *p, const void *q, const void *k,
+                           int32_t *idx, void *ws, size_t ws_bytes, topo_stream_t stream);
+
+/*
+ * The softmax-over-the-set step alone [fr S3]: given index rows idx
+ * [B, Hq, nq, 1+W+k], writes out.  Entries that are negative or outside
+ * 0..p of their row are ignored; every other entry takes part once per
+ * occurrence.  A row with no usable entry gets out = 0.  Needs no workspace.
+ */
+int topo_attn_sparse_softmax_pv(const topo_attn_params *p, const void *q, const void *k,
+                                const void *v, const int32_t *idx, float *out,
+                                topo_stream_t stream);
+
+/* Dense causal attention over keys 0..p (the full-attention "pillar" layer,
+ * [zh S3]); W and k are ignored. */
+int dense_attn_forward(const topo_attn_params *p, const void *q, const void *k, const void *v,
+                       float *out, void *ws, size_t ws_bytes, topo_stream_t stream);
+
+/* Human-readable text of a status code (static storage). */
+const char *topo_attn_strerror(int status);
+
+/* Copy the workspace's device status word to *status (TOPO_OK or
+ * TOPO_ERR_DEVICE_TIMEOUT) and clear it.  Synchronises `stream`. */
+int topo_attn_device_status(void *ws, int *status, topo_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TOPO_ATTN_H */

@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Index sets must match bit for bit; outputs within 1e-5 absolute (float32
+inputs) or 2e-3 row-relative (bfloat16 inputs); the excluded mass within
+1e-6 + 1e-4 * eps.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import dynamic_sparse_transformer_qk_b300 as topo
+from gpu_common import (compare, device_inputs, run_gpu, run_oracle, assert_out_close,
+                        oracle_params)
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+W0 = synth.CONFIGS[0]
+
+
+def _full(w, want_excl=True):
+    x = synth.make(w)
+    g = run_gpu(w, x, want_excl=want_excl)
+    o = run_oracle(w, x, want=("out", "idx", "excl") if want_excl else ("out", "idx"))
+    return compare(w, x, g, o)
+
+
+# ------------------------------------------------------------- workloads ----
+
+def test_tiny_causal_prefill_fp32():
+    """n=2048 fp32 prefill, 1 head, d=64, W=64, k=32: every row."""
+    _full(W0)
+
+
+def test_decode_32k_bf16():
+    """Single-token decode n=32768, 32/8 heads, d=128: every head."""
+    _full(synth.CONFIGS[1])
+
+
+def test_decode_32k_planted_keys_found():
+    w = synth.CONFIGS[1]
+    x = synth.make(w)
+    g = run_gpu(w, x, want_excl=False)
+    for h in range(w.Hq):
+        top = set(g["idx"][h][1:1 + w.k].tolist())
+        assert top == set(x["planted"][(0, h // 4)].tolist())
+
+
+def test_batched_decode_128k_bf16():
+    """B=16 sequences of n=131072: every (sequence, head)."""
+    _full(synth.CONFIGS[2])
+
+
+def test_million_token_decode_bf16():
+    """n=1,048,576 decode, 32/8 heads: every head, plus the dense path."""
+    w = synth.CONFIGS[4]
+    x = synth.make(w)
+    g = run_gpu(w, x, want_excl=True)
+    o = run_oracle(w, x, want=("out", "idx", "excl", "dense"))
+    compare(w, x, g, o)
+    q, k, v = device_inputs(x, w)
+    dense = topo.dense_forward(q, k, v, n=w.n, scale=w.scale)
+    torch.cuda.synchronize()
+    assert_out_close(dense.cpu().numpy().reshape(-1, w.d), o["dense"], w.dtype, "dense")
+
+
+# ------------------------------------------------------------ edge cases ----
+
+EDGE = [
+    # name, overrides of the tiny fp32 prefill workload
+    ("n1", dict(n=1, nq=1)),
+    ("n2_k1", dict(n=2, nq=2, W=1, k=1)),
+    ("window_covers_all", dict(n=50, nq=50, W=64, k=32)),
+    ("k_zero", dict(n=300, nq=300, W=16, k=0)),
+    ("k_exceeds_candidates", dict(n=90, nq=90, W=8, k=200)),
+    ("ragged_tail", dict(n=1000, nq=1000, W=7, k=5)),
+    ("k_256", dict(n=700, nq=700, W=3, k=256)),
+    ("k_100", dict(n=700, nq=700, W=20, k=100)),
+    ("k_60", dict(n=500, nq=500, W=5, k=60)),
+    ("partial_rows", dict(n=777, nq=129, W=10, k=12)),
+    ("decode_row", dict(n=5000, nq=1, W=64, k=32)),
+    ("gqa_2", dict(n=400, nq=400, Hq=4, Hkv=2, W=9, k=7)),
+    ("gqa_3", dict(n=300, nq=37, Hq=6, Hkv=2, W=9, k=7)),
+    ("gqa_8_decode", dict(n=3000, nq=1, Hq=16, Hkv=2, W=33, k=31)),
+    ("gqa_16_decode", dict(n=2000, nq=1, Hq=16, Hkv=1, W=5, k=9)),
+    ("batch_3", dict(B=3, n=333, nq=333, Hq=2, Hkv=1, W=4, k=6)),
+    ("d128_f32", dict(d=128, n=600, nq=600, W=12, k=10)),
+    ("kv_stride_nan_tail", dict(n=555, nq=555, kv_stride=700, nan_tail=True, W=6, k=9)),
+    ("bf16_d64", dict(dtype="bf16", n=800, nq=800, W=11, k=13)),
+    ("bf16_d128_gqa4", dict(dtype="bf16", d=128, Hq=8, Hkv=2, n=900, nq=900, W=16, k=16)),
+    ("bf16_decode_stride", dict(dtype="bf16", d=128, Hq=32, Hkv=8, n=20000, nq=1,
+                                kv_stride=20100, nan_tail=True, planted=32)),
+]
+
+
+@pytest.mark.parametrize("name,kw", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_cases(name, kw):
+    _full(W0.with_(**kw))
+
+
+# ------------------------------------------------------------------ ties ----
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_equal_keys_pick_lowest_positions(dtype):
+    """Every candidate ties: the lowest positions win, through many buffer
+    compactions and the split merge."""
+    w = W0.with_(dtype=dtype, d=128, Hq=4, Hkv=1, n=6000, nq=3, W=10, k=40)
+    x = synth.make(w)
+    x["k"][:] = x["k"][:, :, 7:8, :]
+    g = run_gpu(w, x)
+    o = run_oracle(w, x)
+    compare(w, x, g, o)
+    for row in g["idx"]:
+        assert row[1:41].tolist() == list(range(1, 41))
+
+
+def test_integer_scores_with_many_ties():
+    rng = np.random.default_rng(4)
+    w = W0.with_(d=64, Hq=2, Hkv=1, n=3000, nq=40, W=6, k=24)
+    x = synth.make(w)
+    x["q"][:] = rng.integers(-1, 2, size=x["q"].shape).astype(np.float32)
+    x["k"][:] = rng.integers(-1, 2, size=x["k"].shape).astype(np.float32)
+    g = run_gpu(w, x)
+    o = run_oracle(w, x)
+    compare(w, x, g, o)
+
+
+def test_increasing_scores_stress_compaction():
+    """Scores rise with position: every key beats the running threshold."""
+    w = W0.with_(n=20000, nq=2, W=4, k=33)
+    x = synth.make(w)
+    x["q"][:] = 0.0
+    x["q"][..., 0] = 1.0
+    x["k"][0, 0, :, 0] = np.arange(w.n, dtype=np.float32) * 1e-3
+    g = run_gpu(w, x)
+    o = run_oracle(w, x)
+    compare(w, x, g, o)
+
+
+# ------------------------------------------------- the separate entry points
+
+def test_score_select_and_sparse_softmax_pv():
+    w = W0.with_(dtype="bf16", d=128, Hq=8, Hkv=2, n=1500, nq=40, W=20, k=24)
+    x = synth.make(w)
+    o = run_oracle(w, x, want=("out", "idx"))
+    q, k, v = device_inputs(x, w)
+    idx = topo.score_select(q, k, W=w.W, topk=w.k, n=w.n, scale=w.scale)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy().reshape(o["idx"].shape), o["idx"])
+    # the softmax step on the oracle's own sets
+    oidx = torch.from_numpy(o["idx"].reshape(idx.shape)).cuda()
+    out = topo.sparse_softmax_pv(q, k, v, oidx, W=w.W, topk=w.k, n=w.n, scale=w.scale)
+    torch.cuda.synchronize()
+    assert_out_close(out.cpu().numpy().reshape(-1, w.d), o["out"], w.dtype)
+
+
+def test_sparse_softmax_pv_ignores_out_of_range_entries():
+    w = W0.with_(n=200, nq=200, W=4, k=4)
+    x = synth.make(w)
+    o = run_oracle(w, x, want=("out", "idx"))
+    bad = o["idx"].copy()
+    # -1 pads already present; add positions beyond the row and negatives
+    bad[:, -1] = np.where(bad[:, -1] < 0, 10 ** 6, bad[:, -1])
+    bad[:, -2] = np.where(bad[:, -2] < 0, -7, bad[:, -2])
+    q, k, v = device_inputs(x, w)
+    out = topo.sparse_softmax_pv(q, k, v, torch.from_numpy(bad.reshape(1, 1, w.nq, -1)).cuda(),
+                                 W=w.W, topk=w.k, n=w.n, scale=w.scale)
+    torch.cuda.synchronize()
+    assert_out_close(out.cpu().numpy().reshape(-1, w.d), o["out"], w.dtype)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(dtype="bf16", d=128, Hq=8, Hkv=2),
+                                dict(n=3000, nq=1, Hq=4, Hkv=1), dict(n=1, nq=1)])
+def test_dense_matches_oracle(kw):
+    w = W0.with_(n=700, nq=700).with_(**kw)
+    x = synth.make(w)
+    o = run_oracle(w, x, want=("dense",))
+    q, k, v = device_inputs(x, w)
+    out = topo.dense_forward(q, k, v, n=w.n, scale=w.scale)
+    torch.cuda.synchronize()
+    assert_out_close(out.cpu().numpy().reshape(-1, w.d), o["dense"], w.dtype, "dense")
+
+
+def test_chunked_prefill_equals_full_prefill():
+    w = W0.with_(dtype="bf16", d=128, Hq=8, Hkv=2, n=4096, nq=4096, W=64, k=32, planted=16,
+                 planted_range="all")
+    x = synth.make(w)
+    q, k, v = device_inputs(x, w)
+    full_out, full_idx, _ = topo.forward(q, k, v, W=w.W, topk=w.k, n=w.n, scale=w.scale,
+                                         want_idx=True)
+    chunk = 1024
+    for c in range(w.n // chunk):
+        qc = q[:, :, c * chunk:(c + 1) * chunk].contiguous()
+        out, idx, _ = topo.forward(qc, k, v, W=w.W, topk=w.k, n=(c + 1) * chunk,
+                                   scale=w.scale, want_idx=True)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, full_idx[:, :, c * chunk:(c + 1) * chunk])
+        assert torch.allclose(out, full_out[:, :, c * chunk:(c + 1) * chunk], rtol=0, atol=1e-6)
+
+
+def test_chunked_prefill_sampled_rows():
+    """The chunked prefill workload shape (n=65536, 32/8 heads, chunks of 4096),
+    W=64: sampled rows of every chunk against the oracle."""
+    w = synth.CONFIGS[3].with_(W=64)
+    x = synth.make(w)
+    q, k, v = device_inputs(x, w)
+    rng = np.random.default_rng(20260211)
+    chunk = w.chunk
+    got_idx = np.empty((w.Hq, w.n, 1 + w.W + w.k), np.int32)
+    got_out = np.empty((w.Hq, w.n, w.d), np.float32)
+    for c in range(w.n // chunk):
+        qc = q[:, :, c * chunk:(c + 1) * chunk].contiguous()
+        out, idx, _ = topo.forward(qc, k, v, W=w.W, topk=w.k, n=(c + 1) * chunk, scale=w.scale,
+                                   want_idx=True)
+        got_idx[:, c * chunk:(c + 1) * chunk] = idx[0].cpu().numpy()
+        got_out[:, c * chunk:(c + 1) * chunk] = out[0].cpu().numpy()
+    rows = np.sort(rng.choice(w.Hq * w.n, size=256, replace=False))
+    o = oracle.topo_attn(oracle_params(w), x["q"], x["k"], x["v"], rows=rows,
+                         want=("out", "idx"))
+    np.testing.assert_array_equal(got_idx.reshape(-1, 1 + w.W + w.k)[rows], o["idx"])
+    assert_out_close(got_out.reshape(-1, w.d)[rows], o["out"], w.dtype)
+
+
+# ------------------------------------------------ repeatability and status --
+
+def test_repeatable_and_workspace_reusable():
+    w = synth.CONFIGS[1]
+    x = synth.make(w)
+    ws = topo.Workspace()
+    a = run_gpu(w, x, workspace=ws)
+    b = run_gpu(w, x, workspace=ws)
+    c = run_gpu(w.with_(n=w.n - 1000), x, workspace=ws)  # another shape on the same workspace
+    d = run_gpu(w, x, workspace=ws)
+    for key in ("out", "idx", "excl"):
+        assert np.array_equal(a[key], b[key]) and np.array_equal(a[key], d[key])
+    assert c["idx"].shape == a["idx"].shape
+    assert topo.device_status(ws) == 0
