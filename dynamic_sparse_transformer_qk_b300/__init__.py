@@ -145,10 +145,11 @@ def dense_workspace_size(p: Params) -> int:
 
 
 class Workspace:
-    """A zero-initialised device buffer the library may use for scratch.
+    """A device buffer the library uses for scratch (split lists, counters).
 
-    The library leaves it zeroed after every completed call, so one Workspace
-    can serve any number of stream-ordered calls."""
+    It starts zeroed (which clears the sticky status word); each call clears
+    the counters it needs, so one Workspace can serve any number of
+    stream-ordered calls of any shapes."""
 
     def __init__(self, device=None, nbytes: int = 0):
         self.device = torch.device(device or "cuda")

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import subprocess
 import sys
@@ -34,6 +35,25 @@ def _deps():
             + [os.path.abspath(__file__)])
 
 
+def _source_hash() -> str:
+    h = hashlib.sha256()
+    for path in sorted(_deps()):
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + FLAGS).encode())
+    return h.hexdigest()
+
+
+def up_to_date() -> bool:
+    """True when libtopoattn.so was linked from exactly the current sources."""
+    stamp = LIB + ".srchash"
+    if not (os.path.exists(LIB) and os.path.exists(stamp)):
+        return False
+    with open(stamp) as f:
+        return f.read().strip() == _source_hash()
+
+
 def _stale(target: str, deps) -> bool:
     if not os.path.exists(target):
         return True
@@ -55,6 +75,8 @@ def _compile(src: str, verbose: bool) -> str:
 
 def build(verbose: bool = False, jobs: int | None = None) -> str:
     """Compile (if stale) and link libtopoattn.so; returns its path."""
+    if up_to_date():
+        return LIB
     os.makedirs(BUILD, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 1)) as ex:
@@ -66,6 +88,8 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.check_call(cmd)
         os.replace(tmp, LIB)
+    with open(LIB + ".srchash", "w") as f:
+        f.write(_source_hash() + "\n")
     return LIB
 
 

@@ -2,7 +2,9 @@
 // argument checks, launch planning, workspace layout, TMA descriptors and
 // kernel dispatch.  No allocation, no synchronisation (except the explicit
 // status read-back), no global mutable state beyond lazily resolved driver
-// entry points and per-kernel attribute set-up.
+// entry points and per-kernel attribute set-up.  Each call clears the split
+// counters it uses (one cudaMemsetAsync on the caller's stream), so a
+// workspace may be shared by calls of any shapes, in stream order.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
@@ -260,6 +262,9 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
   G.nsplit_max = P.nsplit;
   G.stages = P.stages;
   G.flags = (out ? topo::kDoPV : 0) | (idx ? topo::kDoIdx : 0) | (excl ? topo::kSaveThr : 0);
+  // the split counters of both passes start at zero on every call
+  rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_lists - P.off_cnt, st));
+  if (rc != TOPO_OK) return rc;
   const dim3 grid((unsigned)(P.ncb * P.nsplit), (unsigned)p->Hkv, (unsigned)p->B);
   rc = dispatch(P.bf16, P.D, [&](auto L) { return L.select(P.NC, P.KE, mk, G, grid, P.smem, st); });
   if (rc != TOPO_OK || !excl) return rc;
@@ -354,6 +359,8 @@ int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, 
   G.stages = P.stages;
   const dim3 grid((unsigned)(P.ncb * P.nsplit), (unsigned)p->Hkv, (unsigned)p->B);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_part - P.off_cnt, st));
+  if (rc != TOPO_OK) return rc;
   return dispatch(P.bf16, P.D, [&](auto L) { return L.dense(P.NC, mk, mv, G, grid, P.smem, st); });
 }
 

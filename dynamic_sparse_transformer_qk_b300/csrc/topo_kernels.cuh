@@ -315,10 +315,7 @@ __device__ __forceinline__ bool finish_split(int* counter, int nsplit, volatile 
   }
   __syncthreads();
   const bool last = misc[1] != 0;
-  if (last) {
-    __threadfence();
-    if (threadIdx.x == 0) *counter = 0;  // ready for the next call
-  }
+  if (last) __threadfence();
   return last;
 }
 

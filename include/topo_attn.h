@@ -47,10 +47,12 @@
  *     unspecified (but memory-safe) results.
  *   - Workspace: `ws` is a caller-owned device buffer of at least
  *     topo_attn_workspace_size() (resp. dense_attn_workspace_size()) bytes,
- *     256-byte aligned.  It must be zero-filled once before its first use
- *     (topo_attn_workspace_init); every call that completes leaves it ready
- *     for the next one.  Calls sharing one workspace must be ordered on one
- *     stream.  After a TOPO_ERR_DEVICE_TIMEOUT report, zero it again.
+ *     256-byte aligned.  Each call clears the part it needs on `stream`
+ *     (one small cudaMemsetAsync), so one workspace may serve calls of any
+ *     shapes.  Its first 4 bytes are a sticky device status word (see
+ *     topo_attn_device_status): zero them once when the buffer is created,
+ *     for instance with topo_attn_workspace_init.  Calls sharing one
+ *     workspace must be ordered on one stream.
  */
 #ifndef TOPO_ATTN_H
 #define TOPO_ATTN_H
@@ -99,7 +101,8 @@ size_t topo_attn_workspace_size(const topo_attn_params *p);
 /* Workspace bytes needed by dense_attn_forward; 0 if invalid. */
 size_t dense_attn_workspace_size(const topo_attn_params *p);
 
-/* Zero `bytes` of workspace on `stream` (cudaMemsetAsync). */
+/* Zero `bytes` of a new workspace on `stream` (cudaMemsetAsync), including
+ * its status word. */
 int topo_attn_workspace_init(void *ws, size_t bytes, topo_stream_t stream);
 
 /*
