@@ -240,7 +240,7 @@ def bench_ours(args, w: synth.Workload):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
         # keep sampling a moment so short regions still get clock samples
-        if t_wall < 0.5:
+        if t_wall < 0.5 and not args.profile:
             extra = max(1, int(0.5 / max(t_wall / args.steps, 1e-6)))
             for _ in range(min(extra, 20000)):
                 step()
@@ -272,6 +272,11 @@ def bench_ours(args, w: synth.Workload):
                 "timing": "CUDA events around each step (one counter memset + one kernel)",
                 "traffic": traffic_from_profile("topo_select_kernel", "decode-1m")}
 
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile": True, "ms_per_step": ms, "value": value,
+                              "workload": workload_desc(w)}), flush=True)
+        return
     # end to end through the public API: pinned host q and the appended K/V
     # row go up, out comes back, every step
     hq = torch.from_numpy(x["q"]).pin_memory()
@@ -368,10 +373,19 @@ def main():
     ap.add_argument("--no-dense", dest="dense", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--n", type=int, default=0,
+                    help="override the causal length (profiling runs on smaller caches)")
+    ap.add_argument("--profile", action="store_true",
+                    help="time the steps only: no e2e, dense, clock padding or CPU baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = synth.CONFIGS[WORKLOADS[args.workload]]
+    if args.n:
+        w = w.with_(n=args.n, name=f"{w.name} (n overridden to {args.n})")
+    if args.profile:
+        args.dense = False
+        args.no_cpu_baseline = True
     if args.impl == "reference":
         bench_reference(args, w)
     else:
