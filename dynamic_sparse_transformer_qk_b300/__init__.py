@@ -25,7 +25,7 @@ import threading
 
 import torch
 
-__all__ = ["forward", "score_select", "sparse_softmax_pv", "dense_forward", "Workspace",
+__all__ = ["forward", "forward_noalloc", "score_select", "sparse_softmax_pv", "dense_forward", "Workspace",
            "TopoError", "library_path", "load_library", "workspace_size", "dense_workspace_size",
            "device_status", "EXPORTS"]
 
@@ -37,7 +37,8 @@ _lib = None
 # every entry point the header declares
 EXPORTS = ("topo_attn_workspace_size", "dense_attn_workspace_size", "topo_attn_workspace_init",
            "topo_attn_forward", "topo_attn_score_select", "topo_attn_sparse_softmax_pv",
-           "dense_attn_forward", "topo_attn_strerror", "topo_attn_device_status")
+           "dense_attn_forward", "topo_attn_strerror", "topo_attn_device_status",
+           "topo_attn_forward_noalloc")
 
 TOPO_OK = 0
 TOPO_KMAX = 256
@@ -82,6 +83,7 @@ def load_library():
             "dense_attn_forward": (i, [P, vp, vp, vp, vp, vp, sz, vp]),
             "topo_attn_strerror": (ctypes.c_char_p, [i]),
             "topo_attn_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
+            "topo_attn_forward_noalloc": (i, [P, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -267,6 +269,27 @@ def dense_forward(q, k, v, *, n: int | None = None, scale: float | None = None, 
                                 out.data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
     _raise(rc, "dense_attn_forward")
     return out
+
+
+def forward_noalloc(q, k, v, *, W: int, topk: int, n: int | None = None,
+                    scale: float | None = None, out=None, idx=None, excl=None, stream=None):
+    """topo_attn_forward_noalloc: like forward() but the library uses its own
+    fixed device scratch array instead of a workspace.  out / idx / excl are
+    allocated here only when not given; pass them to allocate nothing at all.
+    Calls must not overlap on the GPU (they share the array)."""
+    _check(q, k, v)
+    lib = load_library()
+    p = make_params(q, k, W=W, topk=topk, n=n, scale=scale)
+    B, Hq, nq, d = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q.device)
+    rc = lib.topo_attn_forward_noalloc(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
+                                       v.data_ptr(), out.data_ptr(),
+                                       idx.data_ptr() if idx is not None else None,
+                                       excl.data_ptr() if excl is not None else None,
+                                       _stream(stream))
+    _raise(rc, "topo_attn_forward_noalloc")
+    return out, idx, excl
 
 
 def device_status(ws: Workspace, stream=None) -> int:

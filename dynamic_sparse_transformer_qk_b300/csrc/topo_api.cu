@@ -372,6 +372,8 @@ const char* topo_attn_strerror(int status) {
     case TOPO_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case TOPO_ERR_CUDA: return "a CUDA call failed while enqueueing work";
     case TOPO_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+    case TOPO_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the no-allocation entry point's fixed buffer";
     default: return "unknown status";
   }
 }

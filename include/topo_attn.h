@@ -30,7 +30,8 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
- *     library allocates nothing and keeps no global mutable state; it is
+ *     library allocates nothing and keeps no global mutable state (the one
+ *     exception is topo_attn_forward_noalloc's fixed scratch array); it is
  *     thread-safe.  Work is enqueued on `stream` (a cudaStream_t, 0 = legacy
  *     default stream) and the call returns without synchronising.
  *   - Layouts are row-major with d fastest:
@@ -75,7 +76,9 @@ enum {
   TOPO_ERR_UNSUPPORTED = -2,      /* d, k or dtype outside the supported set */
   TOPO_ERR_WORKSPACE = -3,        /* workspace missing, too small or misaligned */
   TOPO_ERR_CUDA = -4,             /* a CUDA runtime/driver call failed at enqueue time */
-  TOPO_ERR_DEVICE_TIMEOUT = -5    /* a bounded device-side wait gave up (see topo_attn_device_status) */
+  TOPO_ERR_DEVICE_TIMEOUT = -5,   /* a bounded device-side wait gave up (see topo_attn_device_status) */
+  TOPO_ERR_SCRATCH_LIMIT = -6     /* topo_attn_forward_noalloc: the problem needs more scratch than
+                                     TOPO_NOALLOC_SCRATCH_BYTES */
 };
 
 typedef enum { TOPO_F32 = 0, TOPO_BF16 = 1 } topo_dtype;
@@ -137,6 +140,41 @@ int topo_attn_sparse_softmax_pv(const topo_attn_params *p, const void *q, const 
  * [zh S3]); W and k are ignored. */
 int dense_attn_forward(const topo_attn_params *p, const void *q, const void *k, const void *v,
                        float *out, void *ws, size_t ws_bytes, topo_stream_t stream);
+
+/*
+ * topo_attn_forward without a caller-supplied workspace.  (The paper has no
+ * counterpart; this is a deployment convenience of this library.)
+ *
+ * For callers that cannot allocate device memory: plugin hosts that hand an
+ * operator only its input and output buffers, and latency-critical serving
+ * loops where cudaMalloc is not allowed after start-up because it can
+ * synchronise the device.  Same arguments, results and status codes as
+ * topo_attn_forward, minus ws / ws_bytes; q, k, v, out (and idx, excl when
+ * given) are still the caller's device buffers.
+ *
+ * Scratch: a fixed array of TOPO_NOALLOC_SCRATCH_BYTES (8 MiB) inside the
+ * library's device image.  Every GPU on which the library is used holds it
+ * until the process exits.  Problems whose topo_attn_workspace_size exceeds it
+ * are rejected with TOPO_ERR_SCRATCH_LIMIT before anything is enqueued (the
+ * decode shapes fit; long chunked-prefill calls need the regular entry point).
+ * This call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and caches it.  Make that
+ * first call before any stream capture on that device.
+ *
+ * Sharing: every call, on every stream and host thread, uses the same array,
+ * which keeps the previous call's contents; each call clears what must start
+ * at zero on its own stream.  Calls whose GPU work overlaps (different streams
+ * not ordered by events, or concurrent host threads) race on the array and
+ * give undefined results: order them on one stream.  The array's device status
+ * word cannot be read back through this entry point.
+ */
+#define TOPO_NOALLOC_SCRATCH_BYTES (8u << 20)
+int topo_attn_forward_noalloc(const topo_attn_params *p, const void *q, const void *k,
+                              const void *v, float *out, int32_t *idx, float *excl,
+                              topo_stream_t stream);
 
 /* Human-readable text of a status code (static storage). */
 const char *topo_attn_strerror(int status);
