@@ -267,10 +267,10 @@ def bench_ours(args, w: synth.Workload):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
-                "kernel": "topo_select_kernel",
+                "kernel": "topo_select_tc_kernel",
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "timing": "CUDA events around each step (one counter memset + one kernel)",
-                "traffic": traffic_from_profile("topo_select_kernel", "decode-1m")}
+                "traffic": traffic_from_profile("topo_select_tc_kernel", "decode-1m")}
 
     if args.profile:
         if rank == 0:

@@ -1,0 +1,154 @@
+// tc_device.cuh -- fifth-generation tensor core (tcgen05) building blocks for
+// sm_100-class GPUs, written from the PTX ISA: tensor-memory (TMEM)
+// allocation, the shared-memory matrix descriptor, the instruction descriptor
+// of kind::f16 MMAs, MMA issue and completion, and TMEM loads.
+//
+// Operand layout used everywhere here: "K-major with 128-byte swizzle".  An
+// operand tile of R rows x 64 bf16 elements (one 128-byte line per row) is
+// stored row after row, 8-row groups (1024-byte swizzle atoms) back to back,
+// with 16-byte granule g of row r at physical granule g ^ (r & 7) -- exactly
+// what a TMA load with CU_TENSOR_MAP_SWIZZLE_128B and a 128-byte inner box
+// writes.  Rows of d = 128 bf16 are two such tiles ("column chunks") one after
+// the other.  Tiles must start on a 1024-byte boundary.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace topo {
+namespace tc {
+
+// ------------------------------------------------------------ descriptors --
+
+// Shared-memory matrix descriptor (64 bit): start address >> 4 in bits 0-13,
+// leading-dimension byte offset >> 4 in bits 16-29, stride-dimension byte
+// offset >> 4 in bits 32-45, descriptor version 1 in bits 46-47, base offset 0
+// (1024-byte aligned atoms), swizzle mode in bits 61-63 (2 = 128-byte).
+// For K-major swizzled operands the stride offset is the distance between
+// 8-row groups (1024 bytes for dense rows); the leading offset is unused.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of a dense kind::f16 MMA with bf16 A and B, float32
+// accumulator, both operands K-major: D format (bits 4-5) = 1 (f32), A format
+// (bits 7-9) = 1 (bf16), B format (bits 10-12) = 1 (bf16), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ TMEM ---
+
+// Allocate `ncols` TMEM columns (power of two, 32..512) for this CTA; the
+// base address is written to shared memory at `dst`.  Whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Whole warp (the one that allocated).
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- MMA ---
+
+// D[tmem] (+)= A * B^T, one thread issues.  accumulate = false overwrites D.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+      : "memory");
+}
+
+// ------------------------------------------------------------- TMEM loads --
+
+// Thread t of the warp reads TMEM lane (lane field of taddr) + t, columns
+// col .. col+N-1 of taddr, into v[0..N).  Whole warp; the warp may only touch
+// the 32-lane quarter (warp id % 4) of TMEM.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r0, r1, r2, r3;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(taddr)
+               : "memory");
+  v[0] = __uint_as_float(r0);
+  v[1] = __uint_as_float(r1);
+  v[2] = __uint_as_float(r2);
+  v[3] = __uint_as_float(r3);
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Wait until this thread's TMEM loads have landed in its registers.
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of element (row r, column c) of a K-major 128-byte-swizzled
+// bf16 operand with `rows` rows per 64-column chunk.
+__host__ __device__ __forceinline__ uint32_t sw128_offset_bf16(int r, int c, int rows) {
+  const int chunk = c >> 6;
+  const int o = (c & 63) * 2;
+  return (uint32_t)(chunk * rows * 128 + r * 128 + ((((o >> 4) ^ (r & 7))) << 4) + (o & 15));
+}
+
+}  // namespace tc
+}  // namespace topo

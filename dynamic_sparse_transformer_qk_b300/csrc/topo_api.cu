@@ -22,6 +22,7 @@ constexpr long long kMaxRows = (1LL << 31) - 2 * kTile;  // TMA row coordinate i
 
 struct Plan {
   bool bf16 = false;
+  bool tc = false;  // tensor-core select kernel (bf16, <= 8 columns per KV head, 1 <= k <= 64)
   int D = 0, NC = 1, KE = 1, KP = 32;
   long long ncols = 0, ncb = 0, units = 0;
   // select (or dense) pass
@@ -69,9 +70,9 @@ int sm_count() {
 
 // Keys per split: enough CTAs to fill every SM, chosen so that the last wave
 // is as full as possible (all splits of a pass take about the same time).
-long long choose_split(long long units, long long nkeys, int slots) {
-  if (nkeys <= kTile) return kTile;
-  const long long smax = nkeys / (4 * kTile) > 1 ? nkeys / (4 * kTile) : 1;
+long long choose_split(long long units, long long nkeys, int slots, long long tile = kTile) {
+  if (nkeys <= tile) return tile;
+  const long long smax = nkeys / (4 * tile) > 1 ? nkeys / (4 * tile) : 1;
   double best = -1.0;
   long long best_s = 1;
   for (long long s = 1; s <= smax && s <= 4096; ++s) {
@@ -84,7 +85,7 @@ long long choose_split(long long units, long long nkeys, int slots) {
     }
     if (total >= 8LL * slots) break;
   }
-  return ceil_div(ceil_div(nkeys, best_s), kTile) * kTile;
+  return ceil_div(ceil_div(nkeys, best_s), tile) * tile;
 }
 
 int stages_for(int stage_bytes, int fixed_bytes, int min_ring) {
@@ -112,9 +113,17 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
   const int tileb = kTile * P->D * es;
   const int slots = sm_count();
   const long long pos_max = p->n - 1;
+  P->tc = !dense && P->bf16 && p->k >= 1 &&
+          ((p->k <= 32 && P->ncols <= 8) || (p->k <= 64 && P->ncols <= 4));
+  if (P->tc) {
+    // tensor-core scorer: all columns of a KV head in one block
+    P->NC = (int)pow2_at_least(P->ncols);
+    P->ncb = 1;
+    P->units = (long long)p->B * p->Hkv;
+  }
   if (!dense) {
     const long long ncand = p->k > 0 ? pos_max - p->W : 0;
-    P->L = choose_split(P->units, ncand > 0 ? ncand : 0, slots);
+    P->L = choose_split(P->units, ncand > 0 ? ncand : 0, slots, P->tc ? topo::kTcTile : kTile);
     P->nsplit = ncand > 0 ? (int)ceil_div(ncand, P->L) : 1;
     const int cap = topo::cap_for(P->KE);
     const topo::Smem base(0, 0, P->D, P->NC, topo::kConsumerWarps * P->NC * cap * 8);
@@ -123,6 +132,15 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
                          : P->NC * P->KP * 4 + topo::kWarps * 2048;
     P->stages = stages_for(tileb + 16, base.total, tail > 32768 ? tail : 32768);
     P->smem = topo::Smem(tileb, P->stages, P->D, P->NC, topo::kConsumerWarps * P->NC * cap * 8).total;
+    if (P->tc) {
+      const int tct = topo::kTcTile * P->D * 2;
+      const int fixed = topo::TcSmem(tct, 0, P->D, P->NC, P->KE).total;
+      int st = (topo::kMaxSmem - fixed) / (tct + 24);
+      if (st > 8) st = 8;
+      if (st < 2) return TOPO_ERR_UNSUPPORTED;
+      P->stages = st;
+      P->smem = topo::TcSmem(tct, st, P->D, P->NC, P->KE).total;
+    }
     // excluded-mass pass: keys 0..p
     P->Le = choose_split(P->units, pos_max + 1, slots);
     P->nsplit_e = (int)ceil_div(pos_max + 1, P->Le);
@@ -178,8 +196,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D map over the rows of k or v ([B*Hkv*kv_stride, d]); box = 128 bytes of
-// one row x 64 rows, 128-byte swizzle.
-int make_map(CUtensorMap* map, const void* base, const topo_attn_params* p) {
+// one row x box_rows rows, 128-byte swizzle.
+int make_map(CUtensorMap* map, const void* base, const topo_attn_params* p,
+             int box_rows = kTile) {
   auto fn = encode_fn();
   if (!fn) return TOPO_ERR_CUDA;
   const bool bf16 = p->dtype == TOPO_BF16;
@@ -187,7 +206,7 @@ int make_map(CUtensorMap* map, const void* base, const topo_attn_params* p) {
   const cuuint64_t rows = (cuuint64_t)p->B * p->Hkv * p->kv_stride;
   const cuuint64_t dims[2] = {(cuuint64_t)p->d, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)p->d * es};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kTile};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
       fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
@@ -266,7 +285,16 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
   rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_lists - P.off_cnt, st));
   if (rc != TOPO_OK) return rc;
   const dim3 grid((unsigned)(P.ncb * P.nsplit), (unsigned)p->Hkv, (unsigned)p->B);
-  rc = dispatch(P.bf16, P.D, [&](auto L) { return L.select(P.NC, P.KE, mk, G, grid, P.smem, st); });
+  if (P.tc) {
+    CUtensorMap mk128;
+    rc = make_map(&mk128, k, p, topo::kTcTile);
+    if (rc != TOPO_OK) return rc;
+    rc = dispatch(P.bf16, P.D,
+                  [&](auto L) { return L.select_tc(P.NC, P.KE, mk128, G, grid, P.smem, st); });
+  } else {
+    rc = dispatch(P.bf16, P.D,
+                  [&](auto L) { return L.select(P.NC, P.KE, mk, G, grid, P.smem, st); });
+  }
   if (rc != TOPO_OK || !excl) return rc;
   Geom E = G;
   E.counters = reinterpret_cast<int*>(w + P.off_cnt_e);

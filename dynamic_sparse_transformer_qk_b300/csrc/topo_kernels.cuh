@@ -380,7 +380,14 @@ __device__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* q
     for (int i = lane; i < cnt; i += 32) {
       const long long j = entry(e0 + i);
       float l = -INFINITY;
-      if (j >= 0) l = G.scale * score_row_global<BF16, D, NC>(G.kp, kvrow0 + j, qd, hc);
+      if (j >= 0) {
+        // start the V row on its way to L2 while the logit is computed
+        const uint8_t* vrow = vbase + (kvrow0 + j) * S::ROWB;
+#pragma unroll
+        for (int o = 0; o < S::ROWB; o += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + o));
+        l = G.scale * score_row_global<BF16, D, NC>(G.kp, kvrow0 + j, qd, hc);
+      }
       wsm[i] = l;
       jsm[i] = (int)j;
       lmax = fmaxf(lmax, l);
@@ -402,8 +409,24 @@ __device__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* q
     for (int e = 0; e < S::EPL; ++e) acc[e] *= alpha;
     mrun = mnew;
     __syncwarp();
-#pragma unroll 4
-    for (int i = 0; i < cnt; ++i) {
+    // gather V in batches of 8 rows so that 8 loads are in flight per lane
+    // (a skipped entry has weight 0 and reads row 0, which always exists)
+    int i = 0;
+    for (; i + 8 <= cnt; i += 8) {
+      float v[8][S::EPL];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = jsm[i + u];
+        lane_elems<BF16, D>(vbase + (kvrow0 + (j >= 0 ? j : 0)) * S::ROWB + lane * S::BPL, v[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = wsm[i + u];
+#pragma unroll
+        for (int e = 0; e < S::EPL; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+      }
+    }
+    for (; i < cnt; ++i) {
       const int j = jsm[i];
       if (j < 0) continue;
       const float w = wsm[i];
@@ -416,6 +439,102 @@ __device__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* q
   }
 #pragma unroll
   for (int e = 0; e < S::EPL; ++e) outp[lane * S::EPL + e] = Z > 0.f ? acc[e] / Z : 0.f;
+}
+
+// Tail of the select kernels, run by the CTA that finished a column block
+// last: merge the splits' exact top-k lists, then per column write C_i, the
+// k-th key (for the excluded-mass pass) and the softmax over C_i.  `run` holds
+// NC * KP keys; `scratch` (>= NC*KP*4 + NW*2048 bytes, and at least one
+// split's lists) is free shared memory.  All threads of the CTA call this;
+// warps 0..NW-1 do the per-column work.
+template <bool BF16, int D, int NC, int KE, int NW>
+__device__ __noinline__ void select_tail(const Geom& G, long long unit, int nsplit, int b, int kvh,
+                                         const ColInfo* cols, const float2* qd, uint64_t* run,
+                                         uint8_t* scratch, int scratch_bytes) {
+  constexpr int KP = 32 * KE;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kk = G.topk;
+  for (int i = tid; i < NC * KP; i += blockDim.x) run[i] = 0ull;
+  const int per_split = NC * KP;  // entries
+  int chunk = scratch_bytes / (per_split * 8);
+  if (chunk < 1) chunk = 1;
+  uint64_t* lbuf = reinterpret_cast<uint64_t*>(scratch);
+  __syncthreads();
+  for (int s0 = 0; s0 < nsplit; s0 += chunk) {
+    const int s1 = s0 + chunk < nsplit ? s0 + chunk : nsplit;
+    const unsigned long long* src = G.lists + ((size_t)unit * G.nsplit_max + s0) * per_split;
+    const int total = (s1 - s0) * per_split;
+    for (int i = tid; i < total; i += blockDim.x) lbuf[i] = __ldcg(src + i);
+    __syncthreads();
+    for (int h = warp; h < NC; h += NW) {
+      if (!cols[h].active) continue;
+      uint64_t a[KE];
+#pragma unroll
+      for (int e = 0; e < KE; ++e) a[e] = run[h * KP + e * 32 + lane];
+      for (int s = 0; s < s1 - s0; ++s) {
+        uint64_t bb[KE];
+#pragma unroll
+        for (int e = 0; e < KE; ++e) bb[e] = lbuf[(size_t)s * per_split + h * KP + e * 32 + lane];
+        warp_merge_desc<KE>(a, bb, lane);
+      }
+#pragma unroll
+      for (int e = 0; e < KE; ++e) run[h * KP + e * 32 + lane] = a[e];
+    }
+    __syncthreads();
+  }
+
+  // per column: C_i, the k-th key, the softmax over C_i
+  int* topj_all = reinterpret_cast<int*>(scratch);
+  float* wsm_all = reinterpret_cast<float*>(scratch + NC * KP * 4);
+  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
+  const long long cmax = 1 + (long long)G.W + kk;
+  for (int h = warp; h < NC; h += NW) {
+    if (!cols[h].active) continue;
+    uint64_t a[KE];
+#pragma unroll
+    for (int e = 0; e < KE; ++e) {
+      const int i = e * 32 + lane;
+      a[e] = i < kk ? run[h * KP + i] : 0ull;
+    }
+    int t = 0;
+#pragma unroll
+    for (int e = 0; e < KE; ++e) t += __popc(__ballot_sync(kFull, a[e] != 0ull));
+    if (G.flags & kSaveThr) {
+      const uint64_t kth = kk > 0 ? warp_list_get<KE>(a, kk - 1) : 0ull;
+      if (lane == 0)
+        G.thr[(size_t)unit * NC + h] = kk == 0 ? ~0ull : (t < kk ? 0ull : kth);
+    }
+    // selected positions, ascending
+    uint64_t y[KE];
+#pragma unroll
+    for (int e = 0; e < KE; ++e) y[e] = a[e] ? (~0ull - (uint64_t)key_pos(a[e])) : 0ull;
+    warp_sort_desc<KE>(y, lane);
+    int* topj = topj_all + h * KP;
+#pragma unroll
+    for (int e = 0; e < KE; ++e) topj[e * 32 + lane] = y[e] ? (int)(~0ull - y[e]) : -1;
+    __syncwarp();
+    const long long p = cols[h].pos;
+    const bool wide = p - G.W + 1 <= 0;  // the window reaches the anchor
+    const long long mEnt = wide ? p + 1 : 1 + t + G.W;
+    const long long wlo = p - G.W + 1;
+    auto entry = [&](long long e) -> long long {
+      if (wide) return e;
+      if (e == 0) return 0;
+      if (e <= t) return topj[e - 1];
+      return wlo + (e - 1 - t);
+    };
+    if (G.flags & kDoIdx) {
+      int* dst = G.idx + cols[h].row * cmax;
+      for (long long e = lane; e < cmax; e += 32) dst[e] = e < mEnt ? (int)entry(e) : -1;
+    }
+    if (G.flags & kDoPV) {
+      float* wsm = wsm_all + warp * 512;
+      int* jsm = reinterpret_cast<int*>(wsm + 256);
+      warp_softmax_pv<BF16, D, NC>(G, kvrow0, qd, h, mEnt, entry, wsm, jsm,
+                                   G.out + cols[h].row * D, lane);
+    }
+    __syncwarp();
+  }
 }
 
 // ================================================== fused select kernel =====
@@ -543,89 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!finish_split(G.counters + unit, nsplit, misc)) return;
 
   // ---------------- tail: this CTA finished the column block last ----------
-  uint64_t* run = wbuf;  // [NC][KP] running merge
-  for (int i = tid; i < NC * KP; i += blockDim.x) run[i] = 0ull;
-  const int ring_bytes = G.stages * S::TILEB;
-  const int per_split = NC * KP;  // entries
-  int chunk = ring_bytes / (per_split * 8);
-  if (chunk < 1) chunk = 1;
-  uint64_t* lbuf = reinterpret_cast<uint64_t*>(ring);
-  __syncthreads();
-  for (int s0 = 0; s0 < nsplit; s0 += chunk) {
-    const int s1 = s0 + chunk < nsplit ? s0 + chunk : nsplit;
-    const unsigned long long* src = G.lists + ((size_t)unit * G.nsplit_max + s0) * per_split;
-    const int total = (s1 - s0) * per_split;
-    for (int i = tid; i < total; i += blockDim.x) lbuf[i] = __ldcg(src + i);
-    __syncthreads();
-    for (int h = warp; h < NC; h += kWarps) {
-      if (!cols[h].active) continue;
-      uint64_t a[KE];
-#pragma unroll
-      for (int e = 0; e < KE; ++e) a[e] = run[h * KP + e * 32 + lane];
-      for (int s = 0; s < s1 - s0; ++s) {
-        uint64_t bb[KE];
-#pragma unroll
-        for (int e = 0; e < KE; ++e) bb[e] = lbuf[(size_t)s * per_split + h * KP + e * 32 + lane];
-        warp_merge_desc<KE>(a, bb, lane);
-      }
-#pragma unroll
-      for (int e = 0; e < KE; ++e) run[h * KP + e * 32 + lane] = a[e];
-    }
-    __syncthreads();
-  }
-
-  // per column: C_i, the k-th key, the softmax over C_i
-  int* topj_all = reinterpret_cast<int*>(ring);
-  float* wsm_all = reinterpret_cast<float*>(ring + NC * KP * 4);
-  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
-  const long long cmax = 1 + (long long)G.W + kk;
-  for (int h = warp; h < NC; h += kWarps) {
-    if (!cols[h].active) continue;
-    uint64_t a[KE];
-#pragma unroll
-    for (int e = 0; e < KE; ++e) {
-      const int i = e * 32 + lane;
-      a[e] = i < kk ? run[h * KP + i] : 0ull;
-    }
-    int t = 0;
-#pragma unroll
-    for (int e = 0; e < KE; ++e) t += __popc(__ballot_sync(kFull, a[e] != 0ull));
-    if (G.flags & kSaveThr) {
-      const uint64_t kth = kk > 0 ? warp_list_get<KE>(a, kk - 1) : 0ull;
-      if (lane == 0)
-        G.thr[(size_t)unit * NC + h] = kk == 0 ? ~0ull : (t < kk ? 0ull : kth);
-    }
-    // selected positions, ascending
-    uint64_t y[KE];
-#pragma unroll
-    for (int e = 0; e < KE; ++e) y[e] = a[e] ? (~0ull - (uint64_t)key_pos(a[e])) : 0ull;
-    warp_sort_desc<KE>(y, lane);
-    int* topj = topj_all + h * KP;
-#pragma unroll
-    for (int e = 0; e < KE; ++e) topj[e * 32 + lane] = y[e] ? (int)(~0ull - y[e]) : -1;
-    __syncwarp();
-    const long long p = cols[h].pos;
-    const bool wide = p - G.W + 1 <= 0;  // the window reaches the anchor
-    const long long mEnt = wide ? p + 1 : 1 + t + G.W;
-    const long long wlo = p - G.W + 1;
-    auto entry = [&](long long e) -> long long {
-      if (wide) return e;
-      if (e == 0) return 0;
-      if (e <= t) return topj[e - 1];
-      return wlo + (e - 1 - t);
-    };
-    if (G.flags & kDoIdx) {
-      int* dst = G.idx + cols[h].row * cmax;
-      for (long long e = lane; e < cmax; e += 32) dst[e] = e < mEnt ? (int)entry(e) : -1;
-    }
-    if (G.flags & kDoPV) {
-      float* wsm = wsm_all + warp * 512;
-      int* jsm = reinterpret_cast<int*>(wsm + 256);
-      warp_softmax_pv<BF16, D, NC>(G, kvrow0, qd, h, mEnt, entry, wsm, jsm,
-                                   G.out + cols[h].row * D, lane);
-    }
-    __syncwarp();
-  }
+  select_tail<BF16, D, NC, KE, kWarps>(G, unit, nsplit, b, kvh, cols, qd, wbuf, ring,
+                                       G.stages * S::TILEB);
 }
 
 // ================================================ excluded-mass pass ========

@@ -2,7 +2,7 @@
 // Each (dtype, d) pair is instantiated in its own translation unit.
 #pragma once
 
-#include "topo_kernels.cuh"
+#include "topo_tc_kernels.cuh"
 
 namespace topo {
 
@@ -24,6 +24,8 @@ struct Launcher {
   static cudaError_t dense(int NC, const CUtensorMap& mk, const CUtensorMap& mv, const Geom& G,
                            dim3 grid, int smem, cudaStream_t st);
   static cudaError_t pv(const Geom& G, long long nrows, cudaStream_t st);
+  static cudaError_t select_tc(int NC, int KE, const CUtensorMap& mk128, const Geom& G, dim3 grid,
+                               int smem, cudaStream_t st);
 };
 
 template <bool BF16, int D, int NC, int KE>
@@ -108,6 +110,42 @@ cudaError_t Launcher<BF16, D>::pv(const Geom& G, long long nrows, cudaStream_t s
   const long long blocks = (nrows + 3) / 4;
   sparse_pv_kernel<BF16, D><<<(unsigned)blocks, 128, 0, st>>>(G);
   return cudaGetLastError();
+}
+
+template <int D, int NC, int KE>
+cudaError_t run_select_tc(const CUtensorMap& mk, const Geom& G, dim3 grid, int smem,
+                          cudaStream_t st) {
+  constexpr auto kern = &topo_select_tc_kernel<D, NC, KE>;
+  const cudaError_t e = allow_smem<kern>();
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTcThreads, smem, st>>>(mk, G);
+  return cudaGetLastError();
+}
+
+template <int D, int NC>
+cudaError_t run_select_tc_ke(int KE, const CUtensorMap& mk, const Geom& G, dim3 grid, int smem,
+                             cudaStream_t st) {
+  if (KE == 1) return run_select_tc<D, NC, 1>(mk, G, grid, smem, st);
+  if constexpr (NC <= 4) {
+    if (KE == 2) return run_select_tc<D, NC, 2>(mk, G, grid, smem, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, const CUtensorMap& mk128, const Geom& G,
+                                         dim3 grid, int smem, cudaStream_t st) {
+  if constexpr (!BF16) {
+    return cudaErrorInvalidValue;
+  } else {
+    switch (NC) {
+      case 1: return run_select_tc_ke<D, 1>(KE, mk128, G, grid, smem, st);
+      case 2: return run_select_tc_ke<D, 2>(KE, mk128, G, grid, smem, st);
+      case 4: return run_select_tc_ke<D, 4>(KE, mk128, G, grid, smem, st);
+      case 8: return run_select_tc_ke<D, 8>(KE, mk128, G, grid, smem, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
 }
 
 extern template struct Launcher<false, 64>;

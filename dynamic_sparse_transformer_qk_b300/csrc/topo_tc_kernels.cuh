@@ -1,0 +1,498 @@
+// topo_tc_kernels.cuh -- tensor-core (tcgen05) scoring for bf16 condensate-set
+// attention with few query columns per KV head (decode).
+//
+// Method ("The Condensate Theorem" explainer pages, technical summary
+// sections 2-3): per query the condensate set is the anchor, the W most recent
+// positions and the top-k remaining positions by q . k, re-identified at every
+// step (every causal key is scored).  The selection must be the exact top-k
+// under the float32 ranking score acc = fma(q[c], k[c], acc), c = 0..d-1.
+//
+// Scoring every key with that float32 chain costs d FMAs per (key, query
+// head) on the CUDA cores.  Here the tensor cores score each 128-key tile
+// against all query columns of the KV head in one MMA (bf16 products are
+// exact, the accumulation is float32 but its rounding is not the chain's),
+// and the exact chain is run only for the few keys that could still be in
+// the top-k:
+//
+//   For a key j and query q, let s_j be the float32 chain and t_j the tensor
+//   core result.  Both are within (gamma_d + beta_d) * sum_c |q_c k_jc| of the
+//   exact dot product (gamma_d = d u / (1 - d u), u = 2^-24, for the chain; the
+//   tensor cores' float32 accumulation is taken to be within beta_d = d 2^-21
+//   relative to the same sum, 64x above what was measured on B300), so
+//   |t_j - s_j| <= delta_j <= F * ||q||_1 * max_c |k_jc|.  Each warp keeps a
+//   candidate buffer ordered by t.  If its k best buffered keys have t >= T,
+//   their exact scores are >= T - delta*, delta* the largest delta seen, so a
+//   key with t_j < T - 2 delta* (hence s_j < T - delta*) is beaten by k keys
+//   and cannot be selected.  Keys above that cut are kept; at the end of the
+//   split the survivors (a few more than k) are rescored with the exact chain
+//   and the exact top-k of the split is published, in the same format the
+//   CUDA-core kernel uses.  If more near-ties than the buffers hold survive
+//   (only with massively repeated scores), the split falls back to scoring
+//   its keys with the exact chain on the CUDA cores.
+//
+// CTA layout: warp 0 lane 0 issues TMA loads of 128-key K tiles (two 128-byte
+// column chunks, 128-byte swizzle) into a ring of stages; warp 1 owns the TMEM
+// accumulators (16 columns per stage) and its lane 0 issues the MMAs
+// (M = 128 keys, N = 16 padded query columns, K = d) and commits them to a
+// per-stage barrier; warps 2..9 are the epilogue, two per TMEM lane quarter,
+// taking alternate tiles: each thread owns one key of the tile, reads its
+// column scores from TMEM and the key row's magnitude from shared memory, then
+// the stage is released and the scores are offered to the warp's buffers.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "tc_device.cuh"
+#include "topo_kernels.cuh"
+
+namespace topo {
+
+constexpr int kTcTile = 128;                  // keys per tile (MMA M)
+constexpr int kTcN = 16;                      // MMA N: query columns, zero padded
+constexpr int kTcEpiWarps = 8;                // epilogue warps
+constexpr int kTcWarps = 2 + kTcEpiWarps;     // + TMA producer + MMA issuer
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr int kTcColsPerStage = kTcN;         // TMEM columns per stage
+
+// candidate buffer entries per warp and column: room for the k-plus-near-ties
+// survivors (2 * 32 * KE) plus one warp's worth of offers
+__host__ __device__ constexpr int tc_cap(int KE) { return KE <= 1 ? 128 : 256; }
+
+// F = 2 (gamma_d + beta_d), with gamma_d rounded up by 1 %; the factor 2 leaves
+// room for the float32 rounding of ||q||_1 and of the threshold itself.
+__host__ __device__ constexpr float tc_delta_factor(int D) {
+  return 2.0f * ((float)D * 5.9604645e-8f * 1.01f + (float)D * 4.76837158e-7f);
+}
+
+// Shared-memory carve-up of the tensor-core select kernel (host and device).
+struct TcSmem {
+  int ring, qtile, bars, qd, buf, wmeta, cols, misc, total;
+  __host__ __device__ TcSmem(int tile_bytes, int stages, int D, int NC, int KE) {
+    int o = 0;
+    ring = o;   o += stages * tile_bytes;          // multiple of 1024
+    qtile = o;  o += kTcN * D * 2;                 // bf16 B operand (1024-aligned)
+    bars = o;   o += 3 * stages * 8;               // full, empty, mma_done
+    o = (o + 15) & ~15;
+    qd = o;     o += D * NC * 8;                   // {q, q} float pairs, [c][col]
+    buf = o;    o += kTcEpiWarps * NC * tc_cap(KE) * 8;
+    wmeta = o;  o += kTcEpiWarps * NC * 8;         // per warp and column: delta*, overflow
+    cols = o;   o += NC * (int)sizeof(ColInfo);
+    misc = o;   o += 64;
+    total = o + 1024;
+  }
+};
+
+struct TcMeta {
+  float delta;
+  int overflow;
+};
+
+// ------------------------------------------------ approximate-key buffer ----
+//
+// A warp's candidate buffer of keys rank_key(t, j) (t: tensor-core score).
+// Sort it, and keep (as a sorted prefix) the entries with t >= T - 2 delta,
+// T the k-th best t; fewer than k entries: keep all (T = -inf).  Returns the
+// kept count and T.
+struct TcKept {
+  int keep;
+  float T;
+};
+
+template <int EC>
+__device__ __noinline__ TcKept tc_compact(uint64_t* buf, int cnt, int k, float two_delta,
+                                          int lane) {
+  __syncwarp();
+  uint64_t x[EC];
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int i = e * 32 + lane;
+    x[e] = i < cnt ? buf[i] : 0ull;
+  }
+  warp_sort_desc<EC>(x, lane);
+  float T = -INFINITY;
+  if (cnt >= k && k > 0) T = key_score(warp_list_get<EC>(x, k - 1));
+  const float cut = T - two_delta;
+  int keep = 0;
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const bool kp = x[e] != 0ull && (T == -INFINITY || key_score(x[e]) >= cut);
+    keep += __popc(__ballot_sync(kFull, kp));
+  }
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int i = e * 32 + lane;
+    buf[i] = i < keep ? x[e] : 0ull;
+  }
+  __syncwarp();
+  return TcKept{keep, T};
+}
+
+template <bool BF16, int D>
+__device__ __forceinline__ float row_magnitude(const uint8_t* tile, int r);
+
+// Largest |k_c| of key row r of a bf16 tile (two 128-byte column chunks per
+// row for d = 128, one for d = 64), read in swizzled order (conflict-free).
+template <>
+__device__ __forceinline__ float row_magnitude<true, 128>(const uint8_t* tile, int r) {
+  __nv_bfloat162 m = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(tile + cc * (kTcTile * 128) + r * 128 +
+                                                      ((g ^ (r & 7)) << 4));
+      m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.x)));
+      m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.y)));
+      m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.z)));
+      m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.w)));
+    }
+  }
+  return fmaxf(__low2float(m), __high2float(m));
+}
+
+template <>
+__device__ __forceinline__ float row_magnitude<true, 64>(const uint8_t* tile, int r) {
+  __nv_bfloat162 m = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + r * 128 + ((g ^ (r & 7)) << 4));
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.x)));
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.y)));
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.z)));
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.w)));
+  }
+  return fmaxf(__low2float(m), __high2float(m));
+}
+
+template <int NL>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NL]);
+template <>
+__device__ __forceinline__ void tmem_ld_cols<4>(uint32_t taddr, float (&v)[4]) {
+  tc::tmem_ld4(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, float (&v)[8]) {
+  tc::tmem_ld8(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, float (&v)[16]) {
+  tc::tmem_ld16(taddr, v);
+}
+
+// ======================================== tensor-core select kernel ==========
+//
+// Grid and workspace as topo_select_kernel (grid.x = column block x split,
+// grid.y = KV head, grid.z = sequence); a split is G.L keys (a multiple of
+// 128).  bf16 only; k <= 32 * KE, KE <= 2; NC <= 8 / KE columns per block.
+template <int D, int NC, int KE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    topo_select_tc_kernel(const __grid_constant__ CUtensorMap map_k, const Geom G) {
+  using S = Shape<true, D>;
+  constexpr int CAP = tc_cap(KE);
+  constexpr int EC = CAP / 32;
+  constexpr int KP = 32 * KE;
+  constexpr int LE = 2 * KE;          // union list length / 32 (k plus near ties)
+  constexpr int LL = 32 * LE;
+  constexpr int TILEB = kTcTile * S::ROWB;
+  constexpr int KSTEPS = D / 16;      // MMA K = 16 bf16 per instruction
+  constexpr int NL = NC <= 4 ? 4 : (NC <= 8 ? 8 : 16);
+  static_assert(NC <= 8 / KE && KE <= 2 && LL + 32 <= CAP && cap_for(KE) <= CAP,
+                "tensor-core select shape");
+
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const long long cb = blockIdx.x / G.nsplit_max;
+  const int split = (int)(blockIdx.x % G.nsplit_max);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kk = G.topk;
+
+  const long long last_col = ((cb + 1) * NC < G.ncols ? (cb + 1) * NC : G.ncols) - 1;
+  const long long pos_max = G.n - G.nq + last_col / G.g;
+  const long long jmax = kk > 0 ? pos_max - G.W : 0;
+  const long long ncand = jmax > 0 ? jmax : 0;
+  const int nsplit = ncand > 0 ? (int)((ncand + G.L - 1) / G.L) : 1;
+  if (split >= nsplit) return;
+  const long long ks = 1 + (long long)split * G.L;
+  const long long ke = (ks + G.L - 1 < jmax) ? ks + G.L - 1 : jmax;  // inclusive
+  const int ntiles = ke >= ks ? (int)((ke - ks + kTcTile) / kTcTile) : 0;
+  const long long unit = ((long long)b * G.Hkv + kvh) * G.ncb + cb;
+  const int stages = G.stages;
+
+  uint8_t* sm = aligned_smem_base();
+  const TcSmem L(TILEB, stages, D, NC, KE);
+  uint8_t* ring = sm + L.ring;
+  uint8_t* qtile = sm + L.qtile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* empty = full + stages;
+  uint64_t* mdone = empty + stages;
+  float2* qd = reinterpret_cast<float2*>(sm + L.qd);
+  uint64_t* wbuf = reinterpret_cast<uint64_t*>(sm + L.buf);
+  TcMeta* meta = reinterpret_cast<TcMeta*>(sm + L.wmeta);
+  ColInfo* cols = reinterpret_cast<ColInfo*>(sm + L.cols);
+  volatile int* misc = reinterpret_cast<volatile int*>(sm + L.misc);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L.misc + 32);
+
+  if (tid == 0) {
+    misc[0] = 0;  // abort
+    misc[1] = 0;  // last CTA of the column block
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+      mbar_init(&mdone[s], 1);
+    }
+    fence_mbar_init();
+  }
+  load_columns<true, D, NC>(G, b, kvh, cb, cols, qd);
+  __syncthreads();
+  // B operand: query columns as bf16 rows (exact: the inputs are bf16), rows
+  // NC..15 zero, K-major with the 128-byte swizzle
+  for (int i = tid; i < kTcN * D; i += blockDim.x) {
+    const int r = i / D, c = i % D;
+    const float x = r < NC ? qd[c * NC + r].x : 0.f;
+    *reinterpret_cast<__nv_bfloat16*>(qtile + tc::sw128_offset_bf16(r, c, kTcN)) =
+        __float2bfloat16_rn(x);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  const uint32_t tmem_cols = 32u < (uint32_t)(stages * kTcColsPerStage)
+                                 ? (stages * kTcColsPerStage <= 64
+                                        ? 64u
+                                        : (stages * kTcColsPerStage <= 128 ? 128u : 256u))
+                                 : 32u;
+  if (warp == 1) {
+    tc::tmem_alloc(tslot, tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  const long long row0 = ((long long)b * G.Hkv + kvh) * G.kv_stride + ks;
+  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ------------------------------------------
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tmap(&map_k);
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        if (misc[0]) break;
+        const int s = t % stages;
+        const uint32_t round = (uint32_t)(t / stages);
+        if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
+          set_status(G.status, kStatusTimeout);
+          misc[0] = 1;
+          break;
+        }
+        uint8_t* dst = ring + (size_t)s * TILEB;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)TILEB);
+        const int y = (int)(row0 + (long long)t * kTcTile);
+#pragma unroll
+        for (int cc = 0; cc < S::NCH; ++cc)
+          tma_load_2d(dst + cc * (kTcTile * 128), &map_k, cc * S::EPC, y, &full[s]);
+      }
+      drain_tiles(t, stages, full, G.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer --------------------------------------------
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTcTile, kTcN);
+      const uint32_t qaddr = smem_addr(qtile);
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        if (misc[0]) break;
+        const int s = t % stages;
+        const uint32_t round = (uint32_t)(t / stages);
+        // the epilogue has released this stage's accumulator, and its tile landed
+        if (!mbar_wait(&empty[s], (round & 1u) ^ 1u) || !mbar_wait(&full[s], round & 1u)) {
+          set_status(G.status, kStatusTimeout);
+          misc[0] = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t aaddr = smem_addr(ring + (size_t)s * TILEB);
+#pragma unroll
+        for (int ks16 = 0; ks16 < KSTEPS; ++ks16) {
+          const uint32_t ao = aaddr + (ks16 >> 2) * (kTcTile * 128) + (ks16 & 3) * 32;
+          const uint32_t bo = qaddr + (ks16 >> 2) * (kTcN * 128) + (ks16 & 3) * 32;
+          tc::mma_bf16(tmem + (uint32_t)(s * kTcColsPerStage), tc::smem_desc_sw128(ao),
+                       tc::smem_desc_sw128(bo), idesc, ks16 > 0);
+        }
+        tc::mma_commit(&mdone[s]);
+      }
+      // no MMA may still be running when the accumulators are freed
+      if (t > 0) {
+        const int tl = t - 1;
+        if (!mbar_wait(&mdone[tl % stages], (uint32_t)(tl / stages) & 1u))
+          set_status(G.status, kStatusTimeout);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------------------------------------
+    const int e = warp - 2;           // 0..7
+    const int half = e >> 2;          // tiles t with t % 2 == half
+    const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;  // this thread's key row in a tile
+    uint64_t* mybuf = wbuf + (size_t)e * NC * CAP;
+    float coef[NC], T[NC], thr[NC];
+    int cnt[NC];
+    bool ovf[NC];
+    long long jh[NC];
+#pragma unroll
+    for (int h = 0; h < NC; ++h) {
+      float a = 0.f;
+      for (int c = lane; c < D; c += 32) a += fabsf(qd[c * NC + h].x);
+      coef[h] = tc_delta_factor(D) * warp_sum(a) * 1.001f;
+      T[h] = -INFINITY;
+      thr[h] = -INFINITY;
+      cnt[h] = 0;
+      ovf[h] = false;
+      jh[h] = cols[h].active ? (cols[h].jhi < ke ? cols[h].jhi : ke) : 0;
+    }
+    float kmag = 0.f;  // largest |k_c| seen by this warp
+    for (int t = half; t < ntiles; t += 2) {
+      const int s = t % stages;
+      const uint32_t round = (uint32_t)(t / stages);
+      const bool ok = __all_sync(kFull, mbar_wait(&mdone[s], round & 1u));
+      if (!ok || misc[0]) {
+        if (!ok && lane == 0) {
+          set_status(G.status, kStatusTimeout);
+          misc[0] = 1;
+        }
+        break;
+      }
+      tc::fence_after_sync();
+      float sc[NL];
+      tmem_ld_cols<NL>(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(s * kTcColsPerStage),
+                       sc);
+      tc::tmem_ld_wait();
+      const long long j = ks + (long long)t * kTcTile + r;
+      const float mk = j <= ke ? row_magnitude<true, D>(ring + (size_t)s * TILEB, r) : 0.f;
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      const float wm = warp_max(mk);
+      if (wm > kmag) {  // larger keys: widen the admission margin
+        kmag = wm;
+#pragma unroll
+        for (int h = 0; h < NC; ++h)
+          if (!ovf[h]) thr[h] = T[h] - 2.f * coef[h] * kmag;
+      }
+#pragma unroll
+      for (int h = 0; h < NC; ++h) {
+        const bool cand = j <= jh[h];
+        bool flag = cand && sc[h] >= thr[h];
+        unsigned mask = __ballot_sync(kFull, flag);
+        if (mask == 0u) continue;
+        uint64_t* hb = mybuf + h * CAP;
+        if (cnt[h] + __popc(mask) > CAP) {
+          const TcKept kept = tc_compact<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
+          cnt[h] = kept.keep;
+          T[h] = kept.T;
+          thr[h] = T[h] - 2.f * coef[h] * kmag;
+          if (cnt[h] + 32 > CAP) {  // the buffer is full of near ties
+            ovf[h] = true;
+            thr[h] = INFINITY;
+          }
+          flag = cand && sc[h] >= thr[h];
+          mask = __ballot_sync(kFull, flag);
+          if (mask == 0u) continue;
+        }
+        if (flag) hb[cnt[h] + __popc(mask & ((1u << lane) - 1u))] = rank_key(sc[h], (uint32_t)j);
+        cnt[h] += __popc(mask);
+      }
+    }
+    // final compaction: each buffer keeps its sorted survivors at [0, LL)
+#pragma unroll 1
+    for (int h = 0; h < NC; ++h) {
+      uint64_t* hb = mybuf + h * CAP;
+      const TcKept kept = tc_compact<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
+      if (kept.keep > LL) ovf[h] = true;
+      if (lane == 0) {
+        meta[e * NC + h].delta = coef[h] * kmag;
+        meta[e * NC + h].overflow = ovf[h] ? 1 : 0;
+      }
+    }
+  }
+  // every role is done with the ring and the accumulators
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, tmem_cols);
+  }
+
+  // ---------------- per column: exact top-k of this split ----------------
+  for (int h = warp - 2; h >= 0 && h < NC; h += kTcEpiWarps) {
+    uint64_t a[LE];
+#pragma unroll
+    for (int ee = 0; ee < LE; ++ee) a[ee] = wbuf[(size_t)h * CAP + ee * 32 + lane];
+    float dmax = meta[h].delta;
+    int ov = meta[h].overflow;
+    for (int w = 1; w < kTcEpiWarps; ++w) {
+      uint64_t bb[LE];
+      const uint64_t* src = wbuf + ((size_t)w * NC + h) * CAP;
+#pragma unroll
+      for (int ee = 0; ee < LE; ++ee) bb[ee] = src[ee * 32 + lane];
+      warp_merge_desc<LE>(a, bb, lane);
+      dmax = fmaxf(dmax, meta[w * NC + h].delta);
+      ov |= meta[w * NC + h].overflow;
+    }
+    // survivors of the union: t >= T - 2 delta*, T its k-th best
+    const float Tu = kk > 0 ? key_score(warp_list_get<LE>(a, kk - 1)) : -INFINITY;
+    const bool haveT = kk > 0 && warp_list_get<LE>(a, kk - 1) != 0ull;
+    const float cut = haveT ? Tu - 2.f * dmax : -INFINITY;
+    const uint64_t lastk = warp_list_get<LE>(a, LL - 1);
+    if (lastk != 0ull && key_score(lastk) >= cut) ov = 1;  // more near ties than slots
+    uint64_t* scratch = wbuf + (size_t)h * CAP;  // this column's warp-0 buffer is free now
+    uint64_t x[LE];
+    if (!ov) {
+      // rescore the survivors with the exact float32 chain
+#pragma unroll
+      for (int ee = 0; ee < LE; ++ee) {
+        const uint64_t key = a[ee];
+        x[ee] = 0ull;
+        if (key != 0ull && key_score(key) >= cut) {
+          const uint32_t jj = key_pos(key);
+          x[ee] = rank_key(score_row_global<true, D, NC>(G.kp, kvrow0 + jj, qd, h), jj);
+        }
+      }
+      warp_sort_desc<LE>(x, lane);
+    } else {
+      // fallback: every key of the split through the exact chain (CUDA cores)
+      constexpr int FEC = cap_for(KE) / 32;
+      uint64_t fthr = 0ull;
+      int fcnt = 0;
+      const long long lim = cols[h].active ? (cols[h].jhi < ke ? cols[h].jhi : ke) : 0;
+      for (long long j0 = ks; j0 <= lim; j0 += 32) {
+        const long long j = j0 + lane;
+        const uint64_t key =
+            j <= lim ? rank_key(score_row_global<true, D, NC>(G.kp, kvrow0 + j, qd, h),
+                                (uint32_t)j)
+                     : 0ull;
+        offer<FEC, KE>(scratch, fthr, fcnt, key, kk, lane);
+      }
+      __syncwarp();
+      uint64_t y[FEC];
+#pragma unroll
+      for (int ee = 0; ee < FEC; ++ee) {
+        const int i = ee * 32 + lane;
+        y[ee] = i < fcnt ? scratch[i] : 0ull;
+      }
+      warp_sort_desc<FEC>(y, lane);
+#pragma unroll
+      for (int ee = 0; ee < LE; ++ee) x[ee] = ee < FEC ? y[ee] : 0ull;
+    }
+    unsigned long long* dst = G.lists + (((size_t)unit * G.nsplit_max + split) * NC + h) * KP;
+#pragma unroll
+    for (int ee = 0; ee < KE; ++ee) {
+      const int i = ee * 32 + lane;
+      dst[i] = (i < kk && cols[h].active) ? x[ee] : 0ull;
+    }
+  }
+  if (!finish_split(G.counters + unit, nsplit, misc)) return;
+  select_tail<true, D, NC, KE, kTcWarps>(G, unit, nsplit, b, kvh, cols, qd, wbuf, ring,
+                                         stages * TILEB);
+}
+
+}  // namespace topo

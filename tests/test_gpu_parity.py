@@ -99,6 +99,68 @@ def test_edge_cases(name, kw):
     _full(W0.with_(**kw))
 
 
+# --------------------------------------- tensor-core scorer (bf16 decode) ----
+# bf16 problems with at most 8 query columns per KV head (4 for k > 32) are
+# scored on the tensor cores with exact rescoring; these shapes cover its
+# column counts, both head sizes, k up to 64, short and multi-tile splits,
+# several sequences and a NaN tail past the causal length.
+
+TC_DECODE = [
+    ("g4_d128_k32", dict(d=128, Hq=32, Hkv=8, n=40000, nq=1, W=64, k=32, planted=32)),
+    ("g1_d64_k1", dict(d=64, Hq=2, Hkv=2, n=3000, nq=1, W=5, k=1)),
+    ("g2_d128_k17", dict(d=128, Hq=4, Hkv=2, n=9000, nq=1, W=100, k=17)),
+    ("g8_d128_k32", dict(d=128, Hq=16, Hkv=2, n=20000, nq=1, W=64, k=32, planted=32)),
+    ("g4_d128_k64", dict(d=128, Hq=8, Hkv=2, n=30000, nq=1, W=64, k=64, planted=32)),
+    ("g2_nq2_k33", dict(d=128, Hq=4, Hkv=2, n=7000, nq=2, W=16, k=33)),
+    ("g2_nq3_k20", dict(d=64, Hq=4, Hkv=2, n=5000, nq=3, W=9, k=20)),
+    ("short", dict(d=128, Hq=8, Hkv=2, n=150, nq=1, W=10, k=32)),
+    ("one_candidate", dict(d=128, Hq=4, Hkv=1, n=66, nq=1, W=64, k=32)),
+    ("batch3", dict(B=3, d=128, Hq=8, Hkv=2, n=12345, nq=1, W=33, k=31, planted=8)),
+    ("nan_tail", dict(d=128, Hq=8, Hkv=2, n=10000, nq=1, kv_stride=10300, nan_tail=True,
+                      W=64, k=32, planted=32)),
+    ("wide_window", dict(d=64, Hq=4, Hkv=1, n=6000, nq=1, W=5000, k=32)),
+]
+
+
+@pytest.mark.parametrize("name,kw", TC_DECODE, ids=[e[0] for e in TC_DECODE])
+def test_tensor_core_decode_shapes(name, kw):
+    _full(W0.with_(dtype="bf16", **kw))
+
+
+@pytest.mark.parametrize("k", [1, 32, 64])
+def test_tensor_core_all_equal_keys_fall_back_exactly(k):
+    """Every candidate has the same score: the tensor-core survivors overflow
+    their buffers and the split is rescored exactly; lowest positions win."""
+    w = W0.with_(dtype="bf16", d=128, Hq=4, Hkv=1, n=30000, nq=1, W=10, k=k)
+    x = synth.make(w)
+    x["k"][:] = x["k"][:, :, 7:8, :]
+    g = run_gpu(w, x)
+    o = run_oracle(w, x)
+    compare(w, x, g, o)
+    for row in g["idx"]:
+        assert row[1:1 + k].tolist() == list(range(1, 1 + k))
+
+
+def test_tensor_core_near_ties():
+    """Keys that differ in one low-order bit: tensor-core rounding cannot
+    separate them, the exact rescoring must."""
+    w = W0.with_(dtype="bf16", d=128, Hq=4, Hkv=1, n=20000, nq=1, W=16, k=32)
+    x = synth.make(w)
+    rng = np.random.default_rng(17)
+    # a key along head 0's query, well above every random key's score
+    q0 = synth.widen(x["q"][0, 0, 0], "bf16").astype(np.float64)
+    base = synth.to_bf16_bits(2.0 * np.sqrt(w.d) * q0 / np.linalg.norm(q0))
+    rows = rng.choice(np.arange(1, w.n - w.W), size=48, replace=False)
+    for r in rows:
+        kr = base.copy()
+        c = int(rng.integers(0, w.d))
+        kr[c] = np.uint16(int(kr[c]) ^ 1)  # flip the lowest mantissa bit of one element
+        x["k"][0, 0, r] = kr
+    g = run_gpu(w, x)
+    o = run_oracle(w, x)
+    compare(w, x, g, o)
+
+
 # ------------------------------------------------------------------ ties ----
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
