@@ -23,6 +23,9 @@ constexpr long long kMaxRows = (1LL << 31) - 2 * kTile;  // TMA row coordinate i
 struct Plan {
   bool bf16 = false;
   bool tc = false;  // tensor-core select kernel (bf16, <= 8 columns per KV head, 1 <= k <= 64)
+  bool pf = false;  // tensor-core chunked-prefill path (bf16, > 8 columns per KV head, k <= 32)
+  int pf_stages = 0, pf_smem = 0, pf_items_per_head = 0, pf_grid = 0, pf_kmax_grid = 1;
+  long long pf_nitems = 0;
   int D = 0, NC = 1, KE = 1, KP = 32;
   long long ncols = 0, ncb = 0, units = 0;
   // select (or dense) pass
@@ -32,7 +35,9 @@ struct Plan {
   long long Le = kTile;
   int nsplit_e = 1, stages_e = 2, smem_e = 0;
   // workspace layout (bytes)
-  size_t off_cnt = 0, off_cnt_e = 0, off_lists = 0, off_thr = 0, off_part = 0, total = 0;
+  size_t off_cnt = 0, off_cnt_e = 0, off_kmax = 0, off_work = 0, off_zero_end = 0;
+  size_t off_lists = 0, off_thr = 0, off_part = 0, off_surv = 0, off_scnt = 0, off_topk = 0;
+  size_t total = 0;
 };
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
@@ -115,6 +120,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
   const long long pos_max = p->n - 1;
   P->tc = !dense && P->bf16 && p->k >= 1 &&
           ((p->k <= 32 && P->ncols <= 8) || (p->k <= 64 && P->ncols <= 4));
+  P->pf = !dense && P->bf16 && !P->tc && p->k >= 1 && p->k <= 32 && P->ncols > 8;
   if (P->tc) {
     // tensor-core scorer: all columns of a KV head in one block
     P->NC = (int)pow2_at_least(P->ncols);
@@ -141,6 +147,22 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
       P->stages = st;
       P->smem = topo::TcSmem(tct, st, P->D, P->NC, P->KE).total;
     }
+    if (P->pf) {
+      const int tile = topo::kPfKeys * P->D * 2;
+      const int fixed = topo::PfSmem(P->D, 0).total;
+      int st = (topo::kMaxSmem - fixed) / (tile + 16);
+      if (st > 8) st = 8;
+      if (st < 2) return TOPO_ERR_UNSUPPORTED;
+      P->pf_stages = st;
+      P->pf_smem = topo::PfSmem(P->D, st).total;
+      P->pf_items_per_head = (int)ceil_div(P->ncols, topo::kPfCols);
+      P->pf_nitems = (long long)p->B * p->Hkv * P->pf_items_per_head;
+      P->pf_grid = (int)(P->pf_nitems < slots ? P->pf_nitems : slots);
+      const long long nvec = p->n * (P->D / 8);
+      long long kg = ceil_div(nvec, 1024);
+      P->pf_kmax_grid = (int)(kg < 1 ? 1 : (kg > 64 ? 64 : kg));
+      if (P->pf_smem > topo::kMaxSmem) return TOPO_ERR_UNSUPPORTED;
+    }
     // excluded-mass pass: keys 0..p
     P->Le = choose_split(P->units, pos_max + 1, slots);
     P->nsplit_e = (int)ceil_div(pos_max + 1, P->Le);
@@ -165,13 +187,27 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
   o = align256(o + (size_t)P->units * 4);
   P->off_cnt_e = o;
   o = align256(o + (size_t)P->units * 4);
+  P->off_kmax = o;
+  o = align256(o + (size_t)p->B * p->Hkv * 4);
+  P->off_work = o;
+  o = align256(o + 4);
+  P->off_zero_end = o;  // everything before this is cleared on every call
   if (!dense) {
     P->off_lists = o;
-    o = align256(o + (size_t)P->units * P->nsplit * P->NC * P->KP * 8);
+    if (!P->pf) o = align256(o + (size_t)P->units * P->nsplit * P->NC * P->KP * 8);
     P->off_thr = o;
     o = align256(o + (size_t)P->units * P->NC * 8);
     P->off_part = o;
     o = align256(o + (size_t)P->units * P->nsplit_e * P->NC * 16);
+    if (P->pf) {
+      const size_t ncolumns = (size_t)p->B * p->Hkv * P->ncols;
+      P->off_surv = o;
+      o = align256(o + ncolumns * topo::kPfLL * 8);
+      P->off_scnt = o;
+      o = align256(o + ncolumns * 4);
+      P->off_topk = o;
+      o = align256(o + ncolumns * p->k * 4);
+    }
   } else {
     P->off_part = o;
     o = align256(o + (size_t)P->units * P->nsplit * P->NC * (P->D + 2) * 4);
@@ -281,11 +317,30 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
   G.nsplit_max = P.nsplit;
   G.stages = P.stages;
   G.flags = (out ? topo::kDoPV : 0) | (idx ? topo::kDoIdx : 0) | (excl ? topo::kSaveThr : 0);
-  // the split counters of both passes start at zero on every call
-  rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_lists - P.off_cnt, st));
+  // split counters, K scales and the work counter start at zero on every call
+  rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_zero_end - P.off_cnt, st));
   if (rc != TOPO_OK) return rc;
   const dim3 grid((unsigned)(P.ncb * P.nsplit), (unsigned)p->Hkv, (unsigned)p->B);
-  if (P.tc) {
+  if (P.pf) {
+    CUtensorMap mk128;
+    rc = make_map(&mk128, k, p, topo::kPfKeys);
+    if (rc != TOPO_OK) return rc;
+    G.kmax = reinterpret_cast<unsigned*>(w + P.off_kmax);
+    G.work = reinterpret_cast<int*>(w + P.off_work);
+    G.surv = reinterpret_cast<unsigned long long*>(w + P.off_surv);
+    G.surv_cnt = reinterpret_cast<int*>(w + P.off_scnt);
+    G.topsel = reinterpret_cast<int*>(w + P.off_topk);
+    G.nitems = P.pf_nitems;
+    G.items_per_head = P.pf_items_per_head;
+    G.thr_nc = P.NC;
+    G.stages = P.pf_stages;
+    if (!excl) G.thr = nullptr;
+    rc = dispatch(P.bf16, P.D, [&](auto L) {
+      return L.prefill(mk128, G, P.pf_grid, P.pf_smem, P.pf_kmax_grid, out != nullptr, st);
+    });
+    G.stages = P.stages;
+    G.thr = reinterpret_cast<unsigned long long*>(w + P.off_thr);
+  } else if (P.tc) {
     CUtensorMap mk128;
     rc = make_map(&mk128, k, p, topo::kTcTile);
     if (rc != TOPO_OK) return rc;

@@ -52,6 +52,15 @@ struct Geom {
   unsigned long long* lists;  // [unit][split][NC][KP]
   unsigned long long* thr;    // [unit][NC]
   float* partials;        // [unit][split][NC][...]
+  // chunked-prefill tensor-core path (topo_prefill.cuh)
+  unsigned* kmax;             // [B*Hkv] float bits of the largest |k_c| over keys 0..n-1
+  unsigned long long* surv;   // [column][kPfLL] surviving candidates (tensor-core keys)
+  int* surv_cnt;              // [column] survivors, -1 when the buffers overflowed
+  int* work;                  // work-queue counter of the scan kernel
+  int* topsel;                // [row][k] selected positions ascending, -1 padded
+  long long nitems;           // scan work items (blocks of 128 columns)
+  int items_per_head;         // blocks per (sequence, KV head)
+  int thr_nc;                 // columns per unit of the excluded-mass pass
 };
 
 struct ColInfo {

@@ -2,7 +2,7 @@
 // Each (dtype, d) pair is instantiated in its own translation unit.
 #pragma once
 
-#include "topo_tc_kernels.cuh"
+#include "topo_prefill.cuh"
 
 namespace topo {
 
@@ -26,6 +26,9 @@ struct Launcher {
   static cudaError_t pv(const Geom& G, long long nrows, cudaStream_t st);
   static cudaError_t select_tc(int NC, int KE, const CUtensorMap& mk128, const Geom& G, dim3 grid,
                                int smem, cudaStream_t st);
+  // chunked prefill on the tensor cores (bf16 only): K scale, scan, finalize, softmax
+  static cudaError_t prefill(const CUtensorMap& mk128, const Geom& G, int scan_grid, int scan_smem,
+                             int kmax_grid, bool do_pv, cudaStream_t st);
 };
 
 template <bool BF16, int D, int NC, int KE>
@@ -145,6 +148,32 @@ cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, const CUtensorMap& mk12
       case 8: return run_select_tc_ke<D, 8>(KE, mk128, G, grid, smem, st);
       default: return cudaErrorInvalidValue;
     }
+  }
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::prefill(const CUtensorMap& mk128, const Geom& G, int scan_grid,
+                                       int scan_smem, int kmax_grid, bool do_pv,
+                                       cudaStream_t st) {
+  if constexpr (!BF16) {
+    return cudaErrorInvalidValue;
+  } else {
+    const dim3 gk((unsigned)kmax_grid, (unsigned)(G.B * G.Hkv));
+    prefill_kmax_kernel<D><<<gk, 256, 0, st>>>(G);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    constexpr auto scan = &prefill_scan_kernel<D>;
+    e = allow_smem<scan>();
+    if (e != cudaSuccess) return e;
+    scan<<<scan_grid, kPfThreads, scan_smem, st>>>(mk128, G);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long ncolumns = (long long)G.B * G.Hkv * G.ncols;
+    prefill_finalize_kernel<D><<<(unsigned)((ncolumns + 3) / 4), 128, 0, st>>>(G);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !do_pv) return e;
+    prefill_pv_kernel<D><<<(unsigned)((ncolumns + 3) / 4), 128, 0, st>>>(G);
+    return cudaGetLastError();
   }
 }
 

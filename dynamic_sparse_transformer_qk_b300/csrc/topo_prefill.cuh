@@ -1,0 +1,546 @@
+// topo_prefill.cuh -- chunked causal prefill of condensate-set attention on
+// the tcgen05 tensor cores (bf16 inputs, many query rows per call).
+//
+// Method ("The Condensate Theorem" explainer pages, technical summary
+// sections 2-3): every query row p selects the anchor 0, the window
+// {p-W+1..p} and the top-k of the keys 1..p-W by q . k (re-identified for every
+// query, so every causal pair is scored), then takes the softmax over that
+// set.  In prefill the scoring of every causal (query, key) pair is a dense
+// contraction: it runs on the tensor cores, and the exact float32 ranking
+// score (acc = fma(q[c], k[c], acc), c = 0..d-1) is recomputed only for the
+// few keys per query that can still be in its top-k.
+//
+// Kernels of one call (launched in this order by topo_api.cu):
+//   prefill_kmax_kernel      largest |k_c| over the causal keys of each KV head
+//                            (the scale of the tensor-core rounding bound);
+//   prefill_scan_kernel      persistent; one work item = 128 query columns
+//                            (query row x head pairs of one KV head) against
+//                            all their candidate keys, 128 keys per tile:
+//                            M = 128 columns (A: queries, resident in shared
+//                            memory), N = 128 keys (B: K tile by TMA), the
+//                            accumulator in TMEM (two buffers).  Each epilogue
+//                            thread owns one column: it keeps a candidate
+//                            buffer in shared memory, appends every score
+//                            above the column's cut and, when a buffer fills,
+//                            the warp compacts its 32 columns one at a time
+//                            (bitonic sort across the warp): the cut becomes
+//                            T - 2 delta, T the column's k-th best tensor-core
+//                            score and delta the bound on |tensor core - exact
+//                            chain| (see topo_tc_kernels.cuh).  Survivors go to
+//                            the workspace;
+//   prefill_finalize_kernel  one warp per column: rescores the survivors with
+//                            the exact chain, keeps the exact top-k (ties to
+//                            the lower position) and writes the sorted top-k,
+//                            C_i (idx) and the k-th key for the excluded-mass
+//                            pass.  A column whose near ties overflowed its
+//                            buffer is rescanned exactly on CUDA cores;
+//   prefill_pv_kernel        one warp per row: float32 online softmax over
+//                            C_i and the weighted sum of V.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "topo_tc_kernels.cuh"
+
+namespace topo {
+
+constexpr int kPfCols = 128;   // query columns per work item (MMA M)
+constexpr int kPfKeys = 128;   // keys per tile (MMA N)
+constexpr int kPfCap = 64;     // candidate slots per column
+constexpr int kPfSub = 8;      // scores offered between room checks
+constexpr int kPfLL = 64;      // survivors published per column
+constexpr int kPfWarps = 6;    // TMA producer, MMA issuer, 4 epilogue warps
+constexpr int kPfThreads = 32 * kPfWarps;
+
+// Shared-memory carve-up of the scan kernel (host and device).
+struct PfSmem {
+  int ring, qtile, bs, bj, bars, misc, total;
+  __host__ __device__ PfSmem(int D, int stages) {
+    const int tile = kPfKeys * D * 2;
+    int o = 0;
+    ring = o;   o += stages * tile;               // multiple of 1024
+    qtile = o;  o += kPfCols * D * 2;             // A operand (1024-aligned)
+    bs = o;     o += kPfCap * kPfCols * 4;        // candidate scores [slot][column]
+    bj = o;     o += kPfCap * kPfCols * 4;        // candidate positions [slot][column]
+    bars = o;   o += (2 * stages + 4) * 8;        // full, empty, acc_full[2], acc_empty[2]
+    misc = o;   o += 64;
+    total = o + 1024;
+  }
+};
+
+// ------------------------------------------------------------- K scale ----
+
+// kmax[b*Hkv + h] = max over keys 0..n-1 and c of |k_c| (float bits; the
+// buffer starts at zero).  grid = (x blocks, B*Hkv), 256 threads.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_kmax_kernel(const Geom G) {
+  const int bh = blockIdx.y;
+  const uint4* base = reinterpret_cast<const uint4*>(G.kp) + (long long)bh * G.kv_stride * (D / 8);
+  const long long nvec = G.n * (D / 8);
+  __nv_bfloat162 m = __floats2bfloat162_rn(0.f, 0.f);
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+       v += (long long)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(base + v);
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.x)));
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.y)));
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.z)));
+    m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w.w)));
+  }
+  float f = warp_max(fmaxf(__low2float(m), __high2float(m)));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = f;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) f = fmaxf(f, red[w]);
+    f = fmaxf(f, red[0]);
+    atomicMax(G.kmax + bh, __float_as_uint(f));  // non-negative floats order as integers
+  }
+}
+
+// ------------------------------------------------------------ scan ---------
+
+// Candidate-buffer state of one column (held by the column's thread).
+struct PfState {
+  int cnt;    // candidates in the buffer
+  float thr;  // scores must exceed this to enter
+  int ovf;    // the buffer filled up with near ties
+};
+
+// Compact the candidate buffers of this warp's 32 columns (one at a time,
+// sorted across the warp).  Keeps, per column, the entries with score >=
+// T - 2 delta (T: its k-th best; all entries while it has fewer than k) as a
+// sorted prefix, and updates the owning lane's count and cut.  `final`
+// compacts overflowed columns too and never flags overflow.
+
+static __device__ __noinline__ PfState pf_compact(float* bs, int* bj, int quarter, int lane, int kk,
+                                                  float two_delta, PfState st, bool final) {
+#pragma unroll 1
+  for (int c = 0; c < 32; ++c) {
+    const int cc = quarter * 32 + c;
+    const int cnt_c = __shfl_sync(kFull, st.cnt, c);
+    const float td = __shfl_sync(kFull, two_delta, c);
+    const bool ov_c = __shfl_sync(kFull, st.ovf, c) != 0;
+    if (ov_c && !final) continue;
+    uint64_t x[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = lane + 32 * r;
+      x[r] = e < cnt_c ? rank_key(bs[e * kPfCols + cc], (uint32_t)bj[e * kPfCols + cc]) : 0ull;
+    }
+    warp_sort_desc<2>(x, lane);
+    float T = -INFINITY;
+    if (kk > 0 && cnt_c >= kk) T = key_score(warp_list_get<2>(x, kk - 1));
+    const float cut = T - td;
+    int keep = 0;
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      keep += __popc(__ballot_sync(kFull, x[r] != 0ull && (T == -INFINITY || key_score(x[r]) >= cut)));
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = lane + 32 * r;
+      if (e < keep) {
+        bs[e * kPfCols + cc] = key_score(x[r]);
+        bj[e * kPfCols + cc] = (int)key_pos(x[r]);
+      }
+    }
+    __syncwarp();
+    if (lane == c) {
+      st.cnt = keep;
+      st.thr = T == -INFINITY ? -INFINITY : cut;
+      if (!final && keep + kPfSub > kPfCap) {  // the buffer is full of near ties
+        st.ovf = 1;
+        st.thr = INFINITY;
+      }
+    }
+  }
+  return st;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_scan_kernel(const __grid_constant__ CUtensorMap map_k, const Geom G) {
+  using S = Shape<true, D>;
+  constexpr int TILEB = kPfKeys * S::ROWB;
+  constexpr int KSTEPS = D / 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int stages = G.stages;
+  const int kk = G.topk;
+
+  uint8_t* sm = aligned_smem_base();
+  const PfSmem L(D, stages);
+  uint8_t* ring = sm + L.ring;
+  uint8_t* qtile = sm + L.qtile;
+  float* bs = reinterpret_cast<float*>(sm + L.bs);
+  int* bj = reinterpret_cast<int*>(sm + L.bj);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* empty = full + stages;
+  uint64_t* accf = empty + stages;
+  uint64_t* acce = accf + 2;
+  volatile int* misc = reinterpret_cast<volatile int*>(sm + L.misc);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L.misc + 32);
+
+  if (tid == 0) {
+    misc[0] = 0;  // abort
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&accf[a], 1);
+      mbar_init(&acce[a], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tslot, 2 * kPfKeys);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  long long seq = 0;  // tiles this CTA has run (phases of the ring and accumulator barriers)
+  const int nbh = G.B * G.Hkv;
+  for (;;) {
+    __syncthreads();
+    if (tid == 0) misc[2] = atomicAdd(G.work, 1);
+    __syncthreads();
+    const long long item = misc[2];
+    if (item >= G.nitems || misc[0]) break;
+    // the longest blocks (latest rows) first
+    const int bh = (int)(item % nbh);
+    const int blk = G.items_per_head - 1 - (int)(item / nbh);
+    const int b = bh / G.Hkv, kvh = bh % G.Hkv;
+    const long long c0 = (long long)blk * kPfCols;
+    const long long cend = (c0 + kPfCols < G.ncols) ? c0 + kPfCols : G.ncols;
+    const long long r_last = (cend - 1) / G.g;
+    const long long jmax = G.n - G.nq + r_last - G.W;
+    const int ntiles = jmax >= 1 ? (int)((jmax + kPfKeys - 1) / kPfKeys) : 0;
+    const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
+
+    // queries of the block: bf16, K-major, 128-byte swizzle; missing columns zero
+    for (int i = tid; i < kPfCols * (D / 8); i += blockDim.x) {
+      const int r = i / (D / 8), v = i % (D / 8);
+      const long long col = c0 + r;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (col < cend) {
+        const long long rr = col / G.g;
+        const int hh = (int)(col % G.g);
+        const long long qrow = ((long long)b * G.Hq + (long long)kvh * G.g + hh) * G.nq + rr;
+        w = __ldg(reinterpret_cast<const uint4*>(G.qp) + qrow * (D / 8) + v);
+      }
+      *reinterpret_cast<uint4*>(qtile + (v >> 3) * (kPfCols * 128) + r * 128 +
+                                (((v & 7) ^ (r & 7)) << 4)) = w;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+
+    if (warp == 0) {
+      // ---------------- TMA producer ----------------------------------------
+      if (lane == 0) {
+        if (ntiles > 0) prefetch_tmap(&map_k);
+        for (int t = 0; t < ntiles; ++t) {
+          if (misc[0]) break;
+          const long long gs = seq + t;
+          const int s = (int)(gs % stages);
+          const uint32_t round = (uint32_t)(gs / stages);
+          if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
+            set_status(G.status, kStatusTimeout);
+            misc[0] = 1;
+            break;
+          }
+          uint8_t* dst = ring + (size_t)s * TILEB;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)TILEB);
+          const int y = (int)(kvrow0 + 1 + (long long)t * kPfKeys);
+#pragma unroll
+          for (int cc = 0; cc < S::NCH; ++cc)
+            tma_load_2d(dst + cc * (kPfKeys * 128), &map_k, cc * S::EPC, y, &full[s]);
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------- MMA issuer --------------------------------------------
+      if (lane == 0) {
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(kPfCols, kPfKeys);
+        const uint32_t qaddr = smem_addr(qtile);
+        for (int t = 0; t < ntiles; ++t) {
+          if (misc[0]) break;
+          const long long gs = seq + t;
+          const int s = (int)(gs % stages);
+          const uint32_t round = (uint32_t)(gs / stages);
+          const int ab = (int)(gs & 1);
+          const uint32_t around = (uint32_t)(gs >> 1);
+          if (!mbar_wait(&acce[ab], (around & 1u) ^ 1u) || !mbar_wait(&full[s], round & 1u)) {
+            set_status(G.status, kStatusTimeout);
+            misc[0] = 1;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t kaddr = smem_addr(ring + (size_t)s * TILEB);
+#pragma unroll
+          for (int ks16 = 0; ks16 < KSTEPS; ++ks16) {
+            const uint32_t off = (ks16 >> 2) * (kPfCols * 128) + (ks16 & 3) * 32;
+            tc::mma_bf16(tmem + (uint32_t)(ab * kPfKeys), tc::smem_desc_sw128(qaddr + off),
+                         tc::smem_desc_sw128(kaddr + off), idesc, ks16 > 0);
+          }
+          tc::mma_commit(&empty[s]);  // the K stage is free once these MMAs are done
+          tc::mma_commit(&accf[ab]);
+        }
+      }
+    } else {
+      // ---------------- epilogue: one column per thread -----------------------
+      const int quarter = warp & 3;
+      const int cl = quarter * 32 + lane;
+      const long long col = c0 + cl;
+      const bool active = col < cend;
+      const long long pos = G.n - G.nq + (active ? col / G.g : 0);
+      const long long jhi = active ? pos - G.W : 0;
+      float qn1 = 0.f;  // ||q||_1 of this column
+#pragma unroll 4
+      for (int v = 0; v < D / 8; ++v) {
+        const uint4 w = *reinterpret_cast<const uint4*>(qtile + (v >> 3) * (kPfCols * 128) +
+                                                        cl * 128 + (((v & 7) ^ (cl & 7)) << 4));
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          qn1 += fabsf(__uint_as_float(u[e] << 16)) + fabsf(__uint_as_float(u[e] & 0xffff0000u));
+      }
+      const float kmx = __uint_as_float(G.kmax[bh]);
+      const float two_delta = 2.f * tc_delta_factor(D) * qn1 * 1.001f * kmx;
+      PfState st{0, -INFINITY, 0};
+      for (int t = 0; t < ntiles; ++t) {
+        const long long gs = seq + t;
+        const int ab = (int)(gs & 1);
+        const uint32_t around = (uint32_t)(gs >> 1);
+        const bool ok = __all_sync(kFull, mbar_wait(&accf[ab], around & 1u));
+        if (!ok || misc[0]) {
+          if (!ok && lane == 0) {
+            set_status(G.status, kStatusTimeout);
+            misc[0] = 1;
+          }
+          break;
+        }
+        tc::fence_after_sync();
+        const long long j0 = 1 + (long long)t * kPfKeys;
+#pragma unroll 1
+        for (int grp = 0; grp < kPfKeys / 32; ++grp) {
+          float sc[32];
+          tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) +
+                            (uint32_t)(ab * kPfKeys + grp * 32),
+                        sc);
+          tc::tmem_ld_wait();
+          if (grp == kPfKeys / 32 - 1) {  // the accumulator buffer is free again
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[ab]);
+          }
+          const long long jg = j0 + grp * 32;
+          if (jg + 31 > jhi) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (jg + i > jhi) sc[i] = -INFINITY;
+          }
+#pragma unroll
+          for (int sub = 0; sub < 32; sub += kPfSub) {
+            if (__any_sync(kFull, !st.ovf && st.cnt + kPfSub > kPfCap))
+              st = pf_compact(bs, bj, quarter, lane, kk, two_delta, st, false);
+#pragma unroll
+            for (int i = sub; i < sub + kPfSub; ++i) {
+              if (sc[i] > st.thr) {
+                bs[st.cnt * kPfCols + cl] = sc[i];
+                bj[st.cnt * kPfCols + cl] = (int)(jg + i);
+                ++st.cnt;
+              }
+            }
+          }
+        }
+      }
+      // survivors of each column, sorted, to the workspace
+      st = pf_compact(bs, bj, quarter, lane, kk, two_delta, st, true);
+#pragma unroll 1
+      for (int c = 0; c < 32; ++c) {
+        const int cc = quarter * 32 + c;
+        if (c0 + cc >= cend) break;
+        const int cnt_c = __shfl_sync(kFull, st.cnt, c);
+        const bool ov_c = __shfl_sync(kFull, st.ovf, c) != 0;
+        const long long gcol = (long long)bh * G.ncols + c0 + cc;
+        unsigned long long* dst = G.surv + gcol * kPfLL;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int e = lane + 32 * r;
+          dst[e] = e < cnt_c ? rank_key(bs[e * kPfCols + cc], (uint32_t)bj[e * kPfCols + cc])
+                             : 0ull;
+        }
+        if (lane == 0) G.surv_cnt[gcol] = ov_c ? -1 : cnt_c;
+      }
+    }
+    seq += ntiles;
+  }
+
+  // no copy into shared memory and no MMA may outlive the CTA
+  if (warp == 0 && lane == 0) {
+    for (long long gs = seq - 1; gs >= 0 && gs >= seq - stages; --gs) {
+      if (!mbar_wait(&empty[gs % stages], (uint32_t)(gs / stages) & 1u))
+        set_status(G.status, kStatusTimeout);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 2 * kPfKeys);
+  }
+}
+
+// ------------------------------------------------------------ finalize -----
+
+// One warp per column (= per output row): exact top-k from the survivors,
+// then the sorted top-k positions, C_i and the k-th key.  4 warps per block.
+template <int D>
+__global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
+  __shared__ float2 qs[4][D];
+  __shared__ uint64_t scratch[4][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gcol = (long long)blockIdx.x * 4 + warp;
+  const long long total = (long long)G.B * G.Hkv * G.ncols;
+  if (gcol >= total) return;
+  const int kk = G.topk;
+  const long long bh = gcol / G.ncols, col = gcol % G.ncols;
+  const int b = (int)(bh / G.Hkv), kvh = (int)(bh % G.Hkv);
+  const long long rr = col / G.g;
+  const int hh = (int)(col % G.g);
+  const long long row = ((long long)b * G.Hq + (long long)kvh * G.g + hh) * G.nq + rr;
+  const long long p = G.n - G.nq + rr;
+  const long long jhi = p - G.W;
+  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
+  for (int c = lane; c < D; c += 32) {
+    const float x = load_elem<true>(G.qp, row * D + c);
+    qs[warp][c] = make_float2(x, x);
+  }
+  __syncwarp();
+  const int cnt = G.surv_cnt[gcol];
+  uint64_t x0;
+  if (cnt >= 0) {
+    uint64_t x[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = lane + 32 * r;
+      const uint64_t key = e < cnt ? G.surv[gcol * kPfLL + e] : 0ull;
+      x[r] = 0ull;
+      if (key != 0ull) {
+        const uint32_t j = key_pos(key);
+        x[r] = rank_key(score_row_global<true, D, 1>(G.kp, kvrow0 + j, qs[warp], 0), j);
+      }
+    }
+    warp_sort_desc<2>(x, lane);
+    x0 = x[0];
+  } else {
+    // the near ties overflowed: every candidate through the exact chain
+    uint64_t fthr = 0ull;
+    int fcnt = 0;
+    uint64_t* sb = scratch[warp];
+    for (long long j0 = 1; j0 <= jhi; j0 += 32) {
+      const long long j = j0 + lane;
+      const uint64_t key =
+          j <= jhi ? rank_key(score_row_global<true, D, 1>(G.kp, kvrow0 + j, qs[warp], 0),
+                              (uint32_t)j)
+                   : 0ull;
+      offer<4, 1>(sb, fthr, fcnt, key, kk, lane);
+    }
+    __syncwarp();
+    uint64_t y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = e * 32 + lane;
+      y[e] = i < fcnt ? sb[i] : 0ull;
+    }
+    warp_sort_desc<4>(y, lane);
+    x0 = y[0];
+  }
+  // x0 at lane i is the i-th best (k <= 32)
+  const uint64_t mine = lane < kk ? x0 : 0ull;
+  const int t = __popc(__ballot_sync(kFull, mine != 0ull));
+  if (G.thr) {
+    const uint64_t kth = __shfl_sync(kFull, x0, (kk > 0 ? kk - 1 : 0) & 31);
+    if (lane == 0) {
+      const long long cb = col / G.thr_nc;
+      const int slot = (int)(col % G.thr_nc);
+      const long long unit = bh * G.ncb + cb;
+      G.thr[(size_t)unit * G.thr_nc + slot] = kk == 0 ? ~0ull : (t < kk ? 0ull : kth);
+    }
+  }
+  // selected positions ascending
+  uint64_t y = mine ? (~0ull - (uint64_t)key_pos(mine)) : 0ull;
+  {
+    uint64_t ya[1] = {y};
+    warp_sort_desc<1>(ya, lane);
+    y = ya[0];
+  }
+  const int tj = y ? (int)(~0ull - y) : -1;
+  if (lane < kk) G.topsel[row * kk + lane] = tj;
+  if (G.idx) {
+    const long long cmax = 1 + (long long)G.W + kk;
+    const bool wide = p - G.W + 1 <= 0;
+    const long long mEnt = wide ? p + 1 : 1 + t + G.W;
+    const long long wlo = p - G.W + 1;
+    int* dst = G.idx + row * cmax;
+    for (long long e0 = 0; e0 < cmax; e0 += 32) {
+      const long long e = e0 + lane;
+      const int from_top = __shfl_sync(kFull, tj, (int)((e - 1) & 31));
+      long long v = -1;
+      if (e < mEnt) {
+        if (wide) v = e;
+        else if (e == 0) v = 0;
+        else if (e <= t) v = from_top;
+        else v = wlo + (e - 1 - t);
+      }
+      if (e < cmax) dst[e] = (int)v;
+    }
+  }
+}
+
+// ------------------------------------------------------------ softmax ------
+
+// One warp per row: softmax over C_i = {0} U top-k U window and the weighted
+// sum of V (4 rows per block).
+template <int D>
+__global__ void __launch_bounds__(128) prefill_pv_kernel(const Geom G) {
+  __shared__ float2 qs[4][D];
+  __shared__ float wsm[4][256];
+  __shared__ int jsm[4][256];
+  __shared__ int tsm[4][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + warp;
+  const long long nrows = (long long)G.B * G.Hq * G.nq;
+  if (row >= nrows) return;
+  const int kk = G.topk;
+  const long long r = row % G.nq;
+  const int h = (int)((row / G.nq) % G.Hq);
+  const int b = (int)(row / (G.nq * G.Hq));
+  const int kvh = h / G.g;
+  const long long p = G.n - G.nq + r;
+  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
+  for (int c = lane; c < D; c += 32) {
+    const float x = load_elem<true>(G.qp, row * D + c);
+    qs[warp][c] = make_float2(x, x);
+  }
+  const int tj = lane < kk ? G.topsel[row * kk + lane] : -1;
+  tsm[warp][lane] = tj;
+  const int t = __popc(__ballot_sync(kFull, tj >= 0));
+  __syncwarp();
+  const bool wide = p - G.W + 1 <= 0;
+  const long long mEnt = wide ? p + 1 : 1 + t + G.W;
+  const long long wlo = p - G.W + 1;
+  const int* top = tsm[warp];
+  auto entry = [&](long long e) -> long long {
+    if (wide) return e;
+    if (e == 0) return 0;
+    if (e <= t) return top[e - 1];
+    return wlo + (e - 1 - t);
+  };
+  warp_softmax_pv<true, D, 1>(G, kvrow0, qs[warp], 0, mEnt, entry, wsm[warp], jsm[warp],
+                              G.out + row * D, lane);
+}
+
+}  // namespace topo

@@ -161,6 +161,40 @@ def test_tensor_core_near_ties():
     compare(w, x, g, o)
 
 
+# ------------------------------------------ tensor-core prefill (bf16, k <= 32)
+# bf16 problems with more than 8 query columns per KV head run the chunked
+# prefill path: scan on the tensor cores, exact rescoring of the survivors,
+# softmax per row.  Shapes cover both head sizes, MHA and GQA up to 8, partial
+# column blocks, several sequences, a NaN tail and windows longer than a tile.
+
+TC_PREFILL = [
+    ("d128_g4_full", dict(d=128, Hq=8, Hkv=2, n=1500, nq=1500, W=64, k=32, planted=16,
+                          planted_range="all")),
+    ("d64_g1", dict(d=64, Hq=3, Hkv=3, n=700, nq=700, W=7, k=5)),
+    ("d128_g8_partial", dict(d=128, Hq=16, Hkv=2, n=2000, nq=33, W=40, k=31)),
+    ("d128_b2_rows", dict(B=2, d=128, Hq=4, Hkv=2, n=3000, nq=300, W=200, k=1)),
+    ("d64_k32_long_window", dict(d=64, Hq=4, Hkv=1, n=2500, nq=2500, W=300, k=32)),
+    ("nan_tail", dict(d=128, Hq=8, Hkv=2, n=1000, nq=1000, kv_stride=1100, nan_tail=True,
+                      W=16, k=24)),
+]
+
+
+@pytest.mark.parametrize("name,kw", TC_PREFILL, ids=[e[0] for e in TC_PREFILL])
+def test_tensor_core_prefill_shapes(name, kw):
+    _full(W0.with_(dtype="bf16", **kw))
+
+
+def test_tensor_core_prefill_all_equal_keys_fall_back_exactly():
+    """Every candidate ties: the column buffers overflow and the finalize step
+    rescans those rows exactly; the lowest positions win."""
+    w = W0.with_(dtype="bf16", d=128, Hq=4, Hkv=1, n=1200, nq=200, W=10, k=32)
+    x = synth.make(w)
+    x["k"][:] = x["k"][:, :, 7:8, :]
+    g = run_gpu(w, x)
+    o = run_oracle(w, x)
+    compare(w, x, g, o)
+
+
 # ------------------------------------------------------------------ ties ----
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
