@@ -179,6 +179,37 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&x)[E], int lane) {
   }
 }
 
+// Sort floats descending across the warp (same network, 32-bit elements).
+template <int E>
+__device__ __forceinline__ void warp_sort_desc_f32(float (&x)[E], int lane) {
+  constexpr int N = 32 * E;
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {
+        const int J = j >> 5;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if (e & J) continue;
+          const bool desc = ((e * 32) & size) == 0;
+          const float a = x[e], b = x[e | J];
+          x[e] = desc ? fmaxf(a, b) : fminf(a, b);
+          x[e | J] = desc ? fminf(a, b) : fmaxf(a, b);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float p = __shfl_xor_sync(kFull, x[e], j);
+          const bool lower = (lane & j) == 0;
+          const bool desc = ((e * 32 + lane) & size) == 0;
+          x[e] = (lower == desc) ? fmaxf(x[e], p) : fminf(x[e], p);
+        }
+      }
+    }
+  }
+}
+
 // a <- the N largest of (a U b), sorted descending; a and b sorted descending.
 // max(a[i], b[N-1-i]) is bitonic and holds exactly those N elements; a
 // half-cleaner cascade then sorts it.

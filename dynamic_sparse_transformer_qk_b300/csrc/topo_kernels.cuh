@@ -54,8 +54,8 @@ struct Geom {
   float* partials;        // [unit][split][NC][...]
   // chunked-prefill tensor-core path (topo_prefill.cuh)
   unsigned* kmax;             // [B*Hkv] float bits of the largest |k_c| over keys 0..n-1
-  unsigned long long* surv;   // [column][kPfLL] surviving candidates (tensor-core keys)
-  int* surv_cnt;              // [column] survivors, -1 when the buffers overflowed
+  unsigned* surv;             // [column][kPfLL] surviving candidates (packed)
+  int* surv_cnt;              // [column] survivors, -1 when the buffer overflowed
   int* work;                  // work-queue counter of the scan kernel
   int* topsel;                // [row][k] selected positions ascending, -1 padded
   long long nitems;           // scan work items (blocks of 128 columns)
@@ -185,6 +185,30 @@ __device__ __forceinline__ float score_row_global(const void* kbase, long long r
 #pragma unroll
     for (int e = 0; e < S::EPV; ++e)
       acc = fmaf(qd[(v * S::EPV + e) * NC + hc].x, chunk_elem<BF16>(w, e), acc);
+  }
+  return acc;
+}
+
+// The same float32 chain with the query as plain floats in shared memory,
+// read four at a time (one broadcast load per four products).
+template <bool BF16, int D>
+__device__ __forceinline__ float score_row_q4(const void* kbase, long long row, const float* q) {
+  using S = Shape<BF16, D>;
+  const uint4* p =
+      reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(kbase) + row * S::ROWB);
+  const float4* q4 = reinterpret_cast<const float4*>(q);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int v = 0; v < S::ROWB / 16; ++v) {
+    const uint4 w = __ldg(p + v);
+#pragma unroll
+    for (int h = 0; h < S::EPV / 4; ++h) {
+      const float4 qq = q4[v * (S::EPV / 4) + h];
+      acc = fmaf(qq.x, chunk_elem<BF16>(w, 4 * h + 0), acc);
+      acc = fmaf(qq.y, chunk_elem<BF16>(w, 4 * h + 1), acc);
+      acc = fmaf(qq.z, chunk_elem<BF16>(w, 4 * h + 2), acc);
+      acc = fmaf(qq.w, chunk_elem<BF16>(w, 4 * h + 3), acc);
+    }
   }
   return acc;
 }
@@ -373,10 +397,9 @@ __device__ __forceinline__ void offer(uint64_t* buf, uint64_t& thr, int& cnt, ui
 // One warp: out = sum_e w_e v_{j(e)} / sum_e w_e over entries e in [0, m) with
 // positions j = entry(e) (negative: skip), w_e = exp(l_e - max l), l_e =
 // scale * (float32 chain q . k_j); float32 online softmax in chunks of 256.
-template <bool BF16, int D, int NC, class Entry>
-__device__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* qd, int hc,
-                                long long m, Entry&& entry, float* wsm, int* jsm, float* outp,
-                                int lane) {
+template <bool BF16, int D, class Entry, class Score>
+__device__ void warp_softmax_pv_with(const Geom& G, long long kvrow0, Score&& score, long long m,
+                                     Entry&& entry, float* wsm, int* jsm, float* outp, int lane) {
   using S = Shape<BF16, D>;
   float mrun = -INFINITY, Z = 0.f;
   float acc[S::EPL];
@@ -395,7 +418,7 @@ __device__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* q
 #pragma unroll
         for (int o = 0; o < S::ROWB; o += 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + o));
-        l = G.scale * score_row_global<BF16, D, NC>(G.kp, kvrow0 + j, qd, hc);
+        l = G.scale * score(kvrow0 + j);
       }
       wsm[i] = l;
       jsm[i] = (int)j;
@@ -448,6 +471,16 @@ __device__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* q
   }
 #pragma unroll
   for (int e = 0; e < S::EPL; ++e) outp[lane * S::EPL + e] = Z > 0.f ? acc[e] / Z : 0.f;
+}
+
+template <bool BF16, int D, int NC, class Entry>
+__device__ __forceinline__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* qd,
+                                                int hc, long long m, Entry&& entry, float* wsm,
+                                                int* jsm, float* outp, int lane) {
+  warp_softmax_pv_with<BF16, D>(
+      G, kvrow0,
+      [&](long long row) { return score_row_global<BF16, D, NC>(G.kp, row, qd, hc); }, m, entry,
+      wsm, jsm, outp, lane);
 }
 
 // Tail of the select kernels, run by the CTA that finished a column block

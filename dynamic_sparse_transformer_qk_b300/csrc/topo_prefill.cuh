@@ -49,19 +49,20 @@ constexpr int kPfKeys = 128;   // keys per tile (MMA N)
 constexpr int kPfCap = 64;     // candidate slots per column
 constexpr int kPfSub = 8;      // scores offered between room checks
 constexpr int kPfLL = 64;      // survivors published per column
-constexpr int kPfWarps = 6;    // TMA producer, MMA issuer, 4 epilogue warps
+constexpr int kPfStride = kPfCols + 1;  // buffer row stride (words): conflict-free both ways
+constexpr int kPfEpiWarps = 4; // one per TMEM lane quarter
+constexpr int kPfWarps = 2 + kPfEpiWarps;  // + TMA producer + MMA issuer
 constexpr int kPfThreads = 32 * kPfWarps;
 
 // Shared-memory carve-up of the scan kernel (host and device).
 struct PfSmem {
-  int ring, qtile, bs, bj, bars, misc, total;
+  int ring, qtile, buf, bars, misc, total;
   __host__ __device__ PfSmem(int D, int stages) {
     const int tile = kPfKeys * D * 2;
     int o = 0;
     ring = o;   o += stages * tile;               // multiple of 1024
     qtile = o;  o += kPfCols * D * 2;             // A operand (1024-aligned)
-    bs = o;     o += kPfCap * kPfCols * 4;        // candidate scores [slot][column]
-    bj = o;     o += kPfCap * kPfCols * 4;        // candidate positions [slot][column]
+    buf = o;    o += 2 * kPfCap * kPfStride * 4;  // scores, then positions [slot][column]
     bars = o;   o += (2 * stages + 4) * 8;        // full, empty, acc_full[2], acc_empty[2]
     misc = o;   o += 64;
     total = o + 1024;
@@ -106,55 +107,105 @@ struct PfState {
   int ovf;    // the buffer filled up with near ties
 };
 
-// Compact the candidate buffers of this warp's 32 columns (one at a time,
-// sorted across the warp).  Keeps, per column, the entries with score >=
-// T - 2 delta (T: its k-th best; all entries while it has fewer than k) as a
-// sorted prefix, and updates the owning lane's count and cut.  `final`
-// compacts overflowed columns too and never flags overflow.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
-static __device__ __noinline__ PfState pf_compact(float* bs, int* bj, int quarter, int lane, int kk,
-                                                  float two_delta, PfState st, bool final) {
-#pragma unroll 1
-  for (int c = 0; c < 32; ++c) {
-    const int cc = quarter * 32 + c;
-    const int cnt_c = __shfl_sync(kFull, st.cnt, c);
-    const float td = __shfl_sync(kFull, two_delta, c);
-    const bool ov_c = __shfl_sync(kFull, st.ovf, c) != 0;
-    if (ov_c && !final) continue;
-    uint64_t x[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e = lane + 32 * r;
-      x[r] = e < cnt_c ? rank_key(bs[e * kPfCols + cc], (uint32_t)bj[e * kPfCols + cc]) : 0ull;
-    }
-    warp_sort_desc<2>(x, lane);
-    float T = -INFINITY;
-    if (kk > 0 && cnt_c >= kk) T = key_score(warp_list_get<2>(x, kk - 1));
-    const float cut = T - td;
-    int keep = 0;
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-      keep += __popc(__ballot_sync(kFull, x[r] != 0ull && (T == -INFINITY || key_score(x[r]) >= cut)));
-    __syncwarp();
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e = lane + 32 * r;
-      if (e < keep) {
-        bs[e * kPfCols + cc] = key_score(x[r]);
-        bj[e * kPfCols + cc] = (int)key_pos(x[r]);
-      }
-    }
-    __syncwarp();
-    if (lane == c) {
-      st.cnt = keep;
-      st.thr = T == -INFINITY ? -INFINITY : cut;
-      if (!final && keep + kPfSub > kPfCap) {  // the buffer is full of near ties
-        st.ovf = 1;
-        st.thr = INFINITY;
-      }
+__device__ __forceinline__ float max8(const float* v) {
+  return fmaxf(max3f(v[0], v[1], v[2]), max3f(v[3], v[4], max3f(v[5], v[6], v[7])));
+}
+
+// Compact the buffer of column c of this warp: T = its k-th best score (the
+// slots sorted across the warp; -inf while it has fewer than k entries), keep
+// the entries with score >= T - 2 delta (in any order) and update lane c's
+// count and cut.  `final` never flags overflow.
+static __device__ __noinline__ PfState pf_compact(float* bs, int* bj, int quarter, int lane,
+                                                  int kk, int c, float two_delta, PfState st,
+                                                  bool final) {
+  const int cc = quarter * 32 + c;
+  const int cnt_c = __shfl_sync(kFull, st.cnt, c);
+  const float td = __shfl_sync(kFull, two_delta, c);
+  const bool h0 = lane < cnt_c, h1 = lane + 32 < cnt_c;
+  const float v0 = h0 ? bs[lane * kPfStride + cc] : -INFINITY;
+  const float v1 = h1 ? bs[(lane + 32) * kPfStride + cc] : -INFINITY;
+  const int j0 = h0 ? bj[lane * kPfStride + cc] : 0;
+  const int j1 = h1 ? bj[(lane + 32) * kPfStride + cc] : 0;
+  float T = -INFINITY;
+  if (kk > 0 && cnt_c >= kk) {
+    float x[2] = {v0, v1};
+    warp_sort_desc_f32<2>(x, lane);
+    const int i = kk - 1;
+    T = __shfl_sync(kFull, (i >> 5) ? x[1] : x[0], i & 31);
+  }
+  const float cut = T - td;
+  const bool k0 = h0 && (T == -INFINITY || v0 >= cut);
+  const bool k1 = h1 && (T == -INFINITY || v1 >= cut);
+  const unsigned b0 = __ballot_sync(kFull, k0), b1 = __ballot_sync(kFull, k1);
+  const unsigned below = (1u << lane) - 1u;
+  const int keep = __popc(b0) + __popc(b1);
+  __syncwarp();
+  if (k0) {
+    const int p = __popc(b0 & below);
+    bs[p * kPfStride + cc] = v0;
+    bj[p * kPfStride + cc] = j0;
+  }
+  if (k1) {
+    const int p = __popc(b0) + __popc(b1 & below);
+    bs[p * kPfStride + cc] = v1;
+    bj[p * kPfStride + cc] = j1;
+  }
+  __syncwarp();
+  if (lane == c) {
+    st.cnt = keep;
+    st.thr = T == -INFINITY ? -INFINITY : cut;
+    if (!final && keep + kPfSub > kPfCap) {  // the buffer is full of near ties
+      st.ovf = 1;
+      st.thr = INFINITY;
     }
   }
   return st;
+}
+
+// Offer 64 consecutive scores (positions jg..jg+63) of this thread's column:
+// the maxima of the eight 8-score groups first (independent), one warp
+// reduction, and the append path only for the groups where some column has a
+// candidate.
+__device__ __forceinline__ void pf_offer64(const float (&sa)[32], const float (&sb)[32],
+                                           long long jg, float* bs, int* bj, int quarter,
+                                           int lane, int cl, int kk, float two_delta,
+                                           PfState& st) {
+  float m[8];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    m[s] = max8(sa + 8 * s);
+    m[4 + s] = max8(sb + 8 * s);
+  }
+  unsigned lm = 0u;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) lm |= (m[s] > st.thr) ? (1u << s) : 0u;
+  const unsigned wm = __reduce_or_sync(kFull, lm);
+  if (wm == 0u) return;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    if (!(wm & (1u << s))) continue;
+    unsigned full = __ballot_sync(kFull, !st.ovf && st.cnt + kPfSub > kPfCap);
+    while (full) {
+      const int c = __ffs(full) - 1;
+      full &= full - 1;
+      st = pf_compact(bs, bj, quarter, lane, kk, c, two_delta, st, false);
+    }
+    const float* v = s < 4 ? sa + 8 * s : sb + 8 * (s - 4);
+#pragma unroll
+    for (int i = 0; i < kPfSub; ++i) {
+      if (v[i] > st.thr) {
+        bs[st.cnt * kPfStride + cl] = v[i];
+        bj[st.cnt * kPfStride + cl] = (int)(jg + 8 * s + i);
+        ++st.cnt;
+      }
+    }
+  }
 }
 
 template <int D>
@@ -171,8 +222,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const PfSmem L(D, stages);
   uint8_t* ring = sm + L.ring;
   uint8_t* qtile = sm + L.qtile;
-  float* bs = reinterpret_cast<float*>(sm + L.bs);
-  int* bj = reinterpret_cast<int*>(sm + L.bj);
+  float* bs = reinterpret_cast<float*>(sm + L.buf);
+  int* bj = reinterpret_cast<int*>(sm + L.buf + kPfCap * kPfStride * 4);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + stages;
   uint64_t* accf = empty + stages;
@@ -188,7 +239,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf[a], 1);
-      mbar_init(&acce[a], 4);
+      mbar_init(&acce[a], kPfEpiWarps);
     }
     fence_mbar_init();
   }
@@ -303,12 +354,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                                         cl * 128 + (((v & 7) ^ (cl & 7)) << 4));
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          qn1 += fabsf(__uint_as_float(u[e] << 16)) + fabsf(__uint_as_float(u[e] & 0xffff0000u));
+        for (int q = 0; q < 4; ++q)
+          qn1 += fabsf(__uint_as_float(u[q] << 16)) + fabsf(__uint_as_float(u[q] & 0xffff0000u));
       }
       const float kmx = __uint_as_float(G.kmax[bh]);
       const float two_delta = 2.f * tc_delta_factor(D) * qn1 * 1.001f * kmx;
       PfState st{0, -INFINITY, 0};
+      const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
       for (int t = 0; t < ntiles; ++t) {
         const long long gs = seq + t;
         const int ab = (int)(gs & 1);
@@ -324,40 +376,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc::fence_after_sync();
         const long long j0 = 1 + (long long)t * kPfKeys;
 #pragma unroll 1
-        for (int grp = 0; grp < kPfKeys / 32; ++grp) {
-          float sc[32];
-          tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) +
-                            (uint32_t)(ab * kPfKeys + grp * 32),
-                        sc);
+        for (int half = 0; half < kPfKeys / 64; ++half) {
+          float sa[32], sb[32];
+          const uint32_t ta = tq + (uint32_t)(ab * kPfKeys + half * 64);
+          tc::tmem_ld32(ta, sa);
+          tc::tmem_ld32(ta + 32, sb);
           tc::tmem_ld_wait();
-          if (grp == kPfKeys / 32 - 1) {  // the accumulator buffer is free again
+          if (half == kPfKeys / 64 - 1) {  // this warp is done with the accumulator
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[ab]);
           }
-          const long long jg = j0 + grp * 32;
-          if (jg + 31 > jhi) {
+          const long long jg = j0 + half * 64;
+          if (jg + 63 > jhi) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (jg + i > jhi) sc[i] = -INFINITY;
-          }
-#pragma unroll
-          for (int sub = 0; sub < 32; sub += kPfSub) {
-            if (__any_sync(kFull, !st.ovf && st.cnt + kPfSub > kPfCap))
-              st = pf_compact(bs, bj, quarter, lane, kk, two_delta, st, false);
-#pragma unroll
-            for (int i = sub; i < sub + kPfSub; ++i) {
-              if (sc[i] > st.thr) {
-                bs[st.cnt * kPfCols + cl] = sc[i];
-                bj[st.cnt * kPfCols + cl] = (int)(jg + i);
-                ++st.cnt;
-              }
+            for (int i = 0; i < 32; ++i) {
+              if (jg + i > jhi) sa[i] = -INFINITY;
+              if (jg + 32 + i > jhi) sb[i] = -INFINITY;
             }
           }
+          pf_offer64(sa, sb, jg, bs, bj, quarter, lane, cl, kk, two_delta, st);
         }
       }
-      // survivors of each column, sorted, to the workspace
-      st = pf_compact(bs, bj, quarter, lane, kk, two_delta, st, true);
+      // survivors of each column (any order) to the workspace
+#pragma unroll 1
+      for (int c = 0; c < 32; ++c)
+        st = pf_compact(bs, bj, quarter, lane, kk, c, two_delta, st, true);
 #pragma unroll 1
       for (int c = 0; c < 32; ++c) {
         const int cc = quarter * 32 + c;
@@ -365,14 +409,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int cnt_c = __shfl_sync(kFull, st.cnt, c);
         const bool ov_c = __shfl_sync(kFull, st.ovf, c) != 0;
         const long long gcol = (long long)bh * G.ncols + c0 + cc;
-        unsigned long long* dst = G.surv + gcol * kPfLL;
+        unsigned* dst = G.surv + gcol * kPfLL;
+        const bool ovl = ov_c || cnt_c > kPfLL;  // more survivors than slots: exact rescan
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int e = lane + 32 * r;
-          dst[e] = e < cnt_c ? rank_key(bs[e * kPfCols + cc], (uint32_t)bj[e * kPfCols + cc])
-                             : 0ull;
+        for (int r = 0; r < kPfLL / 32; ++r) {
+          const int ee = lane + 32 * r;
+          dst[ee] = ee < cnt_c ? (uint32_t)(bj[ee * kPfStride + cc] - 1) : 0u;
         }
-        if (lane == 0) G.surv_cnt[gcol] = ov_c ? -1 : cnt_c;
+        if (lane == 0) G.surv_cnt[gcol] = ovl ? -1 : cnt_c;
       }
     }
     seq += ntiles;
@@ -399,7 +443,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // then the sorted top-k positions, C_i and the k-th key.  4 warps per block.
 template <int D>
 __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
-  __shared__ float2 qs[4][D];
+  __shared__ __align__(16) float qs[4][D];
   __shared__ uint64_t scratch[4][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gcol = (long long)blockIdx.x * 4 + warp;
@@ -414,23 +458,21 @@ __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
   const long long p = G.n - G.nq + rr;
   const long long jhi = p - G.W;
   const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
-  for (int c = lane; c < D; c += 32) {
-    const float x = load_elem<true>(G.qp, row * D + c);
-    qs[warp][c] = make_float2(x, x);
-  }
+  for (int c = lane; c < D; c += 32) qs[warp][c] = load_elem<true>(G.qp, row * D + c);
   __syncwarp();
   const int cnt = G.surv_cnt[gcol];
   uint64_t x0;
   if (cnt >= 0) {
+    // the survivors through the exact chain
     uint64_t x[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int e = lane + 32 * r;
-      const uint64_t key = e < cnt ? G.surv[gcol * kPfLL + e] : 0ull;
+      const int ee = lane + 32 * r;
       x[r] = 0ull;
-      if (key != 0ull) {
-        const uint32_t j = key_pos(key);
-        x[r] = rank_key(score_row_global<true, D, 1>(G.kp, kvrow0 + j, qs[warp], 0), j);
+      if (ee < cnt) {
+        const uint32_t e = G.surv[gcol * kPfLL + ee];
+        const uint32_t j = e + 1u;
+        x[r] = rank_key(score_row_q4<true, D>(G.kp, kvrow0 + j, qs[warp]), j);
       }
     }
     warp_sort_desc<2>(x, lane);
@@ -443,8 +485,7 @@ __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
     for (long long j0 = 1; j0 <= jhi; j0 += 32) {
       const long long j = j0 + lane;
       const uint64_t key =
-          j <= jhi ? rank_key(score_row_global<true, D, 1>(G.kp, kvrow0 + j, qs[warp], 0),
-                              (uint32_t)j)
+          j <= jhi ? rank_key(score_row_q4<true, D>(G.kp, kvrow0 + j, qs[warp]), (uint32_t)j)
                    : 0ull;
       offer<4, 1>(sb, fthr, fcnt, key, kk, lane);
     }
@@ -506,7 +547,7 @@ __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
 // sum of V (4 rows per block).
 template <int D>
 __global__ void __launch_bounds__(128) prefill_pv_kernel(const Geom G) {
-  __shared__ float2 qs[4][D];
+  __shared__ __align__(16) float qs[4][D];
   __shared__ float wsm[4][256];
   __shared__ int jsm[4][256];
   __shared__ int tsm[4][32];
@@ -521,10 +562,7 @@ __global__ void __launch_bounds__(128) prefill_pv_kernel(const Geom G) {
   const int kvh = h / G.g;
   const long long p = G.n - G.nq + r;
   const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
-  for (int c = lane; c < D; c += 32) {
-    const float x = load_elem<true>(G.qp, row * D + c);
-    qs[warp][c] = make_float2(x, x);
-  }
+  for (int c = lane; c < D; c += 32) qs[warp][c] = load_elem<true>(G.qp, row * D + c);
   const int tj = lane < kk ? G.topsel[row * kk + lane] : -1;
   tsm[warp][lane] = tj;
   const int t = __popc(__ballot_sync(kFull, tj >= 0));
@@ -539,8 +577,10 @@ __global__ void __launch_bounds__(128) prefill_pv_kernel(const Geom G) {
     if (e <= t) return top[e - 1];
     return wlo + (e - 1 - t);
   };
-  warp_softmax_pv<true, D, 1>(G, kvrow0, qs[warp], 0, mEnt, entry, wsm[warp], jsm[warp],
-                              G.out + row * D, lane);
+  const float* qw = qs[warp];
+  warp_softmax_pv_with<true, D>(
+      G, kvrow0, [&](long long kr) { return score_row_q4<true, D>(G.kp, kr, qw); }, mEnt, entry,
+      wsm[warp], jsm[warp], G.out + row * D, lane);
 }
 
 }  // namespace topo
