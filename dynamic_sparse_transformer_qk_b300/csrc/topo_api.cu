@@ -29,7 +29,7 @@ struct Plan {
   int D = 0, NC = 1, KE = 1, KP = 32;
   long long ncols = 0, ncb = 0, units = 0;
   // select (or dense) pass
-  long long L = kTile;
+  long long L = kTile, L2 = kTile, hi_units = 0;
   int nsplit = 1, stages = 2, smem = 0;
   // excluded-mass pass
   long long Le = kTile;
@@ -138,6 +138,14 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
                          : P->NC * P->KP * 4 + topo::kWarps * 2048;
     P->stages = stages_for(tileb + 16, base.total, tail > 32768 ? tail : 32768);
     P->smem = topo::Smem(tileb, P->stages, P->D, P->NC, topo::kConsumerWarps * P->NC * cap * 8).total;
+    if (P->tc && P->units * 2 <= slots && ncand > (long long)slots * topo::kTcTile) {
+      // one wave: every unit gets slots/units splits, the first slots%units one more
+      const long long s_lo = slots / P->units;
+      P->hi_units = slots - s_lo * P->units;
+      P->L = ceil_div(ceil_div(ncand, s_lo), topo::kTcTile) * topo::kTcTile;
+      P->L2 = ceil_div(ceil_div(ncand, s_lo + 1), topo::kTcTile) * topo::kTcTile;
+      P->nsplit = (int)ceil_div(ncand, P->hi_units > 0 ? P->L2 : P->L);
+    }
     if (P->tc) {
       const int tct = topo::kTcTile * P->D * 2;
       const int fixed = topo::TcSmem(tct, 0, P->D, P->NC, P->KE).total;
@@ -314,6 +322,8 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
   G.thr = reinterpret_cast<unsigned long long*>(w + P.off_thr);
   G.partials = reinterpret_cast<float*>(w + P.off_part);
   G.L = P.L;
+  G.L2 = P.L2;
+  G.hi_units = P.hi_units;
   G.nsplit_max = P.nsplit;
   G.stages = P.stages;
   G.flags = (out ? topo::kDoPV : 0) | (idx ? topo::kDoIdx : 0) | (excl ? topo::kSaveThr : 0);

@@ -38,6 +38,8 @@ struct Geom {
   long long ncols;        // columns per (sequence, KV head) = nq * g
   long long ncb;          // column blocks per (sequence, KV head)
   long long L;            // keys per split (multiple of kTile)
+  long long L2;           // keys per split of the units below hi_units (tensor-core select)
+  long long hi_units;     // units that use L2 (one more split each); 0: none
   int nsplit_max;         // grid.x = ncb * nsplit_max
   int stages;             // ring depth
   int flags;
@@ -473,6 +475,79 @@ __device__ void warp_softmax_pv_with(const Geom& G, long long kvrow0, Score&& sc
   for (int e = 0; e < S::EPL; ++e) outp[lane * S::EPL + e] = Z > 0.f ? acc[e] / Z : 0.f;
 }
 
+// The float32 chain for one key row held in shared memory (linear layout).
+template <bool BF16, int D, int NC>
+__device__ __forceinline__ float score_row_smem(const uint8_t* krow, const float2* qd, int hc) {
+  using S = Shape<BF16, D>;
+  const uint4* p = reinterpret_cast<const uint4*>(krow);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int v = 0; v < S::ROWB / 16; ++v) {
+    const uint4 w = p[v];
+#pragma unroll
+    for (int e = 0; e < S::EPV; ++e)
+      acc = fmaf(qd[(v * S::EPV + e) * NC + hc].x, chunk_elem<BF16>(w, e), acc);
+  }
+  return acc;
+}
+
+// warp_softmax_pv with every K and V row already staged in shared memory:
+// entry e lives in slot slot_of(e) (negative: skip); slot s holds the K row
+// at stage + s * 2 * ROWB and the V row right after it.
+template <bool BF16, int D, int NC, class Slot>
+__device__ void warp_softmax_pv_staged(const Geom& G, const float2* qd, int hc, long long m,
+                                       Slot&& slot_of, const uint8_t* stage, float* wsm,
+                                       int* jsm, float* outp, int lane) {
+  using S = Shape<BF16, D>;
+  float mrun = -INFINITY, Z = 0.f;
+  float acc[S::EPL];
+#pragma unroll
+  for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
+  for (long long e0 = 0; e0 < m; e0 += 256) {
+    const int cnt = (int)(m - e0 < 256 ? m - e0 : 256);
+    float lmax = -INFINITY;
+    for (int i = lane; i < cnt; i += 32) {
+      const int sl = slot_of(e0 + i);
+      float l = -INFINITY;
+      if (sl >= 0)
+        l = G.scale * score_row_smem<BF16, D, NC>(stage + (size_t)sl * 2 * S::ROWB, qd, hc);
+      wsm[i] = l;
+      jsm[i] = sl;
+      lmax = fmaxf(lmax, l);
+    }
+    lmax = warp_max(lmax);
+    const float mnew = fmaxf(mrun, lmax);
+    __syncwarp();
+    if (mnew == -INFINITY) continue;
+    const float alpha = (mrun == -INFINITY) ? 0.f : expf(mrun - mnew);
+    float zs = 0.f;
+    for (int i = lane; i < cnt; i += 32) {
+      const float l = wsm[i];
+      const float w = (l == -INFINITY) ? 0.f : expf(l - mnew);
+      wsm[i] = w;
+      zs += w;
+    }
+    Z = Z * alpha + warp_sum(zs);
+#pragma unroll
+    for (int e = 0; e < S::EPL; ++e) acc[e] *= alpha;
+    mrun = mnew;
+    __syncwarp();
+#pragma unroll 4
+    for (int i = 0; i < cnt; ++i) {
+      const int sl = jsm[i];
+      if (sl < 0) continue;
+      const float w = wsm[i];
+      float v[S::EPL];
+      lane_elems<BF16, D>(stage + (size_t)sl * 2 * S::ROWB + S::ROWB + lane * S::BPL, v);
+#pragma unroll
+      for (int e = 0; e < S::EPL; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int e = 0; e < S::EPL; ++e) outp[lane * S::EPL + e] = Z > 0.f ? acc[e] / Z : 0.f;
+}
+
 template <bool BF16, int D, int NC, class Entry>
 __device__ __forceinline__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* qd,
                                                 int hc, long long m, Entry&& entry, float* wsm,
@@ -486,9 +561,11 @@ __device__ __forceinline__ void warp_softmax_pv(const Geom& G, long long kvrow0,
 // Tail of the select kernels, run by the CTA that finished a column block
 // last: merge the splits' exact top-k lists, then per column write C_i, the
 // k-th key (for the excluded-mass pass) and the softmax over C_i.  `run` holds
-// NC * KP keys; `scratch` (>= NC*KP*4 + NW*2048 bytes, and at least one
-// split's lists) is free shared memory.  All threads of the CTA call this;
-// warps 0..NW-1 do the per-column work.
+// NC * KP keys; `scratch` (>= NC*KP*4 + NW*2048 + NC*4 bytes, and at least
+// one split's lists) is free shared memory, 1024-byte aligned.  When the rows
+// of the softmax fit behind that, they are staged there by bulk copies;
+// otherwise they are read from global memory.  All threads of the CTA call
+// this; warps 0..NW-1 do the per-column work.
 template <bool BF16, int D, int NC, int KE, int NW>
 __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nsplit, int b, int kvh,
                                          const ColInfo* cols, const float2* qd, uint64_t* run,
@@ -530,6 +607,8 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   float* wsm_all = reinterpret_cast<float*>(scratch + NC * KP * 4);
   const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
   const long long cmax = 1 + (long long)G.W + kk;
+  int* tcount = reinterpret_cast<int*>(scratch + NC * KP * 4 + NW * 2048);  // [NC]
+  // per column: the k-th key, the selected positions (ascending) and C_i
   for (int h = warp; h < NC; h += NW) {
     if (!cols[h].active) continue;
     uint64_t a[KE];
@@ -546,7 +625,6 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       if (lane == 0)
         G.thr[(size_t)unit * NC + h] = kk == 0 ? ~0ull : (t < kk ? 0ull : kth);
     }
-    // selected positions, ascending
     uint64_t y[KE];
 #pragma unroll
     for (int e = 0; e < KE; ++e) y[e] = a[e] ? (~0ull - (uint64_t)key_pos(a[e])) : 0ull;
@@ -554,24 +632,104 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
     int* topj = topj_all + h * KP;
 #pragma unroll
     for (int e = 0; e < KE; ++e) topj[e * 32 + lane] = y[e] ? (int)(~0ull - y[e]) : -1;
+    if (lane == 0) tcount[h] = t;
     __syncwarp();
+    if (G.flags & kDoIdx) {
+      const long long p = cols[h].pos;
+      const bool wide = p - G.W + 1 <= 0;  // the window reaches the anchor
+      const long long mEnt = wide ? p + 1 : 1 + t + G.W;
+      const long long wlo = p - G.W + 1;
+      int* dst = G.idx + cols[h].row * cmax;
+      for (long long e = lane; e < cmax; e += 32) {
+        long long v = -1;
+        if (e < mEnt) v = wide ? e : (e == 0 ? 0 : (e <= t ? topj[e - 1] : wlo + (e - 1 - t)));
+        dst[e] = (int)v;
+      }
+    }
+  }
+  if (!(G.flags & kDoPV)) return;
+  __syncthreads();
+
+  // Stage every K and V row the softmax needs in shared memory with one burst
+  // of bulk copies: the band covering all windows of the block (and the
+  // anchor), then each column's top-k rows.
+  using S = Shape<BF16, D>;
+  long long plo = 0x7fffffffffffffffLL, phi = -1;
+  for (int h = 0; h < NC; ++h)
+    if (cols[h].active) {
+      plo = cols[h].pos < plo ? cols[h].pos : plo;
+      phi = cols[h].pos > phi ? cols[h].pos : phi;
+    }
+  const long long band_lo = plo - G.W + 1 > 0 ? plo - G.W + 1 : 0;
+  const long long nb = phi - band_lo + 1;
+  const long long anchor_slot = band_lo == 0 ? 0 : nb;
+  const long long top0 = nb + 1;
+  const long long nslots = top0 + (long long)NC * kk;
+  const int stage_off = (NC * KP * 4 + NW * 2048 + NC * 4 + 64 + 1023) & ~1023;
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(scratch + stage_off - 64);
+  uint8_t* stage = scratch + stage_off;
+  const bool staged = phi >= 0 && (long long)stage_off + nslots * 2 * S::ROWB <= scratch_bytes;
+  bool ok = true;
+  if (staged) {
+    long long filled = nb + (band_lo == 0 ? 0 : 1);
+    for (int h = 0; h < NC; ++h)
+      if (cols[h].active) filled += tcount[h];
+    if (tid == 0) {
+      mbar_init(sbar, 1);
+      fence_mbar_init();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) mbar_arrive_expect_tx(sbar, (uint32_t)(filled * 2 * S::ROWB));
+    const uint8_t* kb = reinterpret_cast<const uint8_t*>(G.kp);
+    const uint8_t* vb = reinterpret_cast<const uint8_t*>(G.vp);
+    for (long long sl = tid; sl < nslots; sl += blockDim.x) {
+      long long row = -1;
+      if (sl < nb) {
+        row = band_lo + sl;
+      } else if (sl == nb) {
+        row = band_lo == 0 ? -1 : 0;
+      } else {
+        const int h = (int)((sl - top0) / kk), i = (int)((sl - top0) % kk);
+        if (cols[h].active && i < tcount[h]) row = topj_all[h * KP + i];
+      }
+      if (row < 0) continue;
+      uint8_t* dst = stage + (size_t)sl * 2 * S::ROWB;
+      bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, sbar);
+      bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, sbar);
+    }
+    ok = mbar_wait(sbar, 0);
+    if (!ok && tid == 0) set_status(G.status, kStatusTimeout);
+    __syncthreads();
+  }
+
+  // per column: the softmax over C_i and the weighted sum of V
+  for (int h = warp; h < NC; h += NW) {
+    if (!cols[h].active || !ok) continue;
+    const int t = tcount[h];
+    const int* topj = topj_all + h * KP;
     const long long p = cols[h].pos;
-    const bool wide = p - G.W + 1 <= 0;  // the window reaches the anchor
+    const bool wide = p - G.W + 1 <= 0;
     const long long mEnt = wide ? p + 1 : 1 + t + G.W;
     const long long wlo = p - G.W + 1;
-    auto entry = [&](long long e) -> long long {
-      if (wide) return e;
-      if (e == 0) return 0;
-      if (e <= t) return topj[e - 1];
-      return wlo + (e - 1 - t);
-    };
-    if (G.flags & kDoIdx) {
-      int* dst = G.idx + cols[h].row * cmax;
-      for (long long e = lane; e < cmax; e += 32) dst[e] = e < mEnt ? (int)entry(e) : -1;
-    }
-    if (G.flags & kDoPV) {
-      float* wsm = wsm_all + warp * 512;
-      int* jsm = reinterpret_cast<int*>(wsm + 256);
+    float* wsm = wsm_all + warp * 512;
+    int* jsm = reinterpret_cast<int*>(wsm + 256);
+    if (staged) {
+      auto slot_of = [&](long long e) -> int {
+        if (wide) return (int)(e - band_lo);  // 0..p lies in the band, which starts at 0
+        if (e == 0) return (int)anchor_slot;
+        if (e <= t) return (int)(top0 + (long long)h * kk + (e - 1));
+        return (int)(wlo + (e - 1 - t) - band_lo);
+      };
+      warp_softmax_pv_staged<BF16, D, NC>(G, qd, h, mEnt, slot_of, stage, wsm, jsm,
+                                          G.out + cols[h].row * D, lane);
+    } else {
+      auto entry = [&](long long e) -> long long {
+        if (wide) return e;
+        if (e == 0) return 0;
+        if (e <= t) return topj[e - 1];
+        return wlo + (e - 1 - t);
+      };
       warp_softmax_pv<BF16, D, NC>(G, kvrow0, qd, h, mEnt, entry, wsm, jsm,
                                    G.out + cols[h].row * D, lane);
     }

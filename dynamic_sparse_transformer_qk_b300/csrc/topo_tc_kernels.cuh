@@ -210,12 +210,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const long long pos_max = G.n - G.nq + last_col / G.g;
   const long long jmax = kk > 0 ? pos_max - G.W : 0;
   const long long ncand = jmax > 0 ? jmax : 0;
-  const int nsplit = ncand > 0 ? (int)((ncand + G.L - 1) / G.L) : 1;
-  if (split >= nsplit) return;
-  const long long ks = 1 + (long long)split * G.L;
-  const long long ke = (ks + G.L - 1 < jmax) ? ks + G.L - 1 : jmax;  // inclusive
-  const int ntiles = ke >= ks ? (int)((ke - ks + kTcTile) / kTcTile) : 0;
   const long long unit = ((long long)b * G.Hkv + kvh) * G.ncb + cb;
+  const long long Lu = unit < G.hi_units ? G.L2 : G.L;  // keys per split of this unit
+  const int nsplit = ncand > 0 ? (int)((ncand + Lu - 1) / Lu) : 1;
+  if (split >= nsplit) return;
+  const long long ks = 1 + (long long)split * Lu;
+  const long long ke = (ks + Lu - 1 < jmax) ? ks + Lu - 1 : jmax;  // inclusive
+  const int ntiles = ke >= ks ? (int)((ke - ks + kTcTile) / kTcTile) : 0;
   const int stages = G.stages;
 
   uint8_t* sm = aligned_smem_base();
