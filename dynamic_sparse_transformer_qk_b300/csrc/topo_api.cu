@@ -93,6 +93,27 @@ long long choose_split(long long units, long long nkeys, int slots, long long ti
   return ceil_div(ceil_div(nkeys, best_s), tile) * tile;
 }
 
+// Keys per split for the tensor-core select kernel: minimises the estimated
+// time waves x (keys per split + fixed), where `fixed` is the per-CTA cost
+// (set-up, exact rescoring and publishing) expressed in keys streamed.
+long long choose_split_tc(long long units, long long nkeys, int slots, long long fixed) {
+  const long long tile = topo::kTcTile;
+  if (nkeys <= tile) return tile;
+  double best = 1e300;
+  long long best_l = ceil_div(nkeys, tile) * tile;
+  for (long long s = 1; s <= 4096 && (s - 1) * tile < nkeys; ++s) {
+    const long long l = ceil_div(ceil_div(nkeys, s), tile) * tile;
+    const long long nsp = ceil_div(nkeys, l);
+    const long long waves = ceil_div(units * nsp, slots);
+    const double cost = (double)waves * (double)(l + fixed);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_l = l;
+    }
+  }
+  return best_l;
+}
+
 int stages_for(int stage_bytes, int fixed_bytes, int min_ring) {
   int st = (topo::kMaxSmem - fixed_bytes) / stage_bytes;
   if (st > 16) st = 16;
@@ -129,7 +150,8 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
   }
   if (!dense) {
     const long long ncand = p->k > 0 ? pos_max - p->W : 0;
-    P->L = choose_split(P->units, ncand > 0 ? ncand : 0, slots, P->tc ? topo::kTcTile : kTile);
+    P->L = P->tc ? choose_split_tc(P->units, ncand > 0 ? ncand : 0, slots, 1200)
+                 : choose_split(P->units, ncand > 0 ? ncand : 0, slots);
     P->nsplit = ncand > 0 ? (int)ceil_div(ncand, P->L) : 1;
     const int cap = topo::cap_for(P->KE);
     const topo::Smem base(0, 0, P->D, P->NC, topo::kConsumerWarps * P->NC * cap * 8);

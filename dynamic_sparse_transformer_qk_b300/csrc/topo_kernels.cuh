@@ -180,13 +180,15 @@ __device__ __forceinline__ float score_row_global(const void* kbase, long long r
   using S = Shape<BF16, D>;
   const uint4* p =
       reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(kbase) + row * S::ROWB);
+  uint4 w[S::ROWB / 16];  // every load of the row in flight at once
+#pragma unroll
+  for (int v = 0; v < S::ROWB / 16; ++v) w[v] = __ldg(p + v);
   float acc = 0.f;
-#pragma unroll 4
+#pragma unroll
   for (int v = 0; v < S::ROWB / 16; ++v) {
-    const uint4 w = __ldg(p + v);
 #pragma unroll
     for (int e = 0; e < S::EPV; ++e)
-      acc = fmaf(qd[(v * S::EPV + e) * NC + hc].x, chunk_elem<BF16>(w, e), acc);
+      acc = fmaf(qd[(v * S::EPV + e) * NC + hc].x, chunk_elem<BF16>(w[v], e), acc);
   }
   return acc;
 }
@@ -561,53 +563,130 @@ __device__ __forceinline__ void warp_softmax_pv(const Geom& G, long long kvrow0,
 // Tail of the select kernels, run by the CTA that finished a column block
 // last: merge the splits' exact top-k lists, then per column write C_i, the
 // k-th key (for the excluded-mass pass) and the softmax over C_i.  `run` holds
-// NC * KP keys; `scratch` (>= NC*KP*4 + NW*2048 + NC*4 bytes, and at least
-// one split's lists) is free shared memory, 1024-byte aligned.  When the rows
-// of the softmax fit behind that, they are staged there by bulk copies;
-// otherwise they are read from global memory.  All threads of the CTA call
-// this; warps 0..NW-1 do the per-column work.
+// NC * KP keys; `scratch` (1024-byte aligned, at least NC*KP*4 + NC*8 + 1024
+// + NW*2048 bytes and one split's lists) is free shared memory.
+//
+// Fast path, when everything fits in `scratch`: the lists of all splits come
+// in with one bulk copy; the rows every softmax needs (the band covering the
+// block's windows and the anchor, then each column's top-k) are staged with
+// bulk copies, the band ones issued before the merge; logits are computed by
+// all threads, then one thread per (column, output element) forms the
+// weighted sum of V.  Otherwise the lists are read in chunks and one warp per
+// column reads its rows from global memory.  All threads of the CTA call this;
+// warps 0..NW-1 do the per-column work.
 template <bool BF16, int D, int NC, int KE, int NW>
 __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nsplit, int b, int kvh,
                                          const ColInfo* cols, const float2* qd, uint64_t* run,
                                          uint8_t* scratch, int scratch_bytes) {
+  using S = Shape<BF16, D>;
   constexpr int KP = 32 * KE;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kk = G.topk;
-  for (int i = tid; i < NC * KP; i += blockDim.x) run[i] = 0ull;
+  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
+  const long long cmax = 1 + (long long)G.W + kk;
+
+  // fixed part of the scratch
+  int* topj_all = reinterpret_cast<int*>(scratch);                       // [NC][KP]
+  int* tcount = reinterpret_cast<int*>(scratch + NC * KP * 4);            // [NC]
+  float* zsum = reinterpret_cast<float*>(scratch + NC * KP * 4 + NC * 4); // [NC]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      scratch + ((NC * KP * 4 + NC * 8 + 15) & ~15));                     // lists, band, top-k
+  const int v0 = (NC * KP * 4 + NC * 8 + 32 + 1023) & ~1023;
+  // variable part: lists | logits | staged rows
   const int per_split = NC * KP;  // entries
-  int chunk = scratch_bytes / (per_split * 8);
-  if (chunk < 1) chunk = 1;
-  uint64_t* lbuf = reinterpret_cast<uint64_t*>(scratch);
-  __syncthreads();
-  for (int s0 = 0; s0 < nsplit; s0 += chunk) {
-    const int s1 = s0 + chunk < nsplit ? s0 + chunk : nsplit;
-    const unsigned long long* src = G.lists + ((size_t)unit * G.nsplit_max + s0) * per_split;
-    const int total = (s1 - s0) * per_split;
-    for (int i = tid; i < total; i += blockDim.x) lbuf[i] = __ldcg(src + i);
+  const long long list_bytes = (long long)nsplit * per_split * 8;
+  const int off_lw = (int)((v0 + list_bytes + 1023) & ~1023LL);
+  const long long mmax = cmax;  // entries per column at most
+  const int off_stage = (int)((off_lw + NC * mmax * 4 + NC * 4 + 1023) & ~1023LL);
+
+  long long plo = 0x7fffffffffffffffLL, phi = -1;
+  for (int h = 0; h < NC; ++h)
+    if (cols[h].active) {
+      plo = cols[h].pos < plo ? cols[h].pos : plo;
+      phi = cols[h].pos > phi ? cols[h].pos : phi;
+    }
+  const long long band_lo = plo - G.W + 1 > 0 ? plo - G.W + 1 : 0;
+  const long long nb = phi - band_lo + 1;
+  const long long anchor_slot = band_lo == 0 ? 0 : nb;
+  const long long top0 = nb + 1;
+  const long long nslots = top0 + (long long)NC * kk;
+  const bool fast = (G.flags & kDoPV) && phi >= 0 &&
+                    (long long)off_stage + nslots * 2 * S::ROWB + (long long)NC * mmax * 4 <=
+                        scratch_bytes;
+  uint8_t* stage = scratch + off_stage;
+  float* lw = reinterpret_cast<float*>(scratch + off_lw);
+  const uint8_t* kb = reinterpret_cast<const uint8_t*>(G.kp);
+  const uint8_t* vb = reinterpret_cast<const uint8_t*>(G.vp);
+
+  for (int i = tid; i < NC * KP; i += blockDim.x) run[i] = 0ull;
+  if (fast) {
+    if (tid == 0) {
+      for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+      fence_mbar_init();
+    }
+    // the split lists were written by other CTAs through the generic proxy
+    asm volatile("fence.proxy.async;" ::: "memory");
     __syncthreads();
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bars[0], (uint32_t)list_bytes);
+      bulk_copy_g2s(scratch + v0, G.lists + (size_t)unit * G.nsplit_max * per_split,
+                    (uint32_t)list_bytes, &bars[0]);
+      mbar_arrive_expect_tx(&bars[1], (uint32_t)((nb + (band_lo == 0 ? 0 : 1)) * 2 * S::ROWB));
+    }
+    // band and anchor rows are known already: start them now
+    for (long long sl = tid; sl < top0; sl += blockDim.x) {
+      long long row = sl < nb ? band_lo + sl : (band_lo == 0 ? -1 : 0);
+      if (row < 0) continue;
+      uint8_t* dst = stage + (size_t)sl * 2 * S::ROWB;
+      bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[1]);
+      bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[1]);
+    }
+    if (!mbar_wait(&bars[0], 0) && tid == 0) set_status(G.status, kStatusTimeout);
     for (int h = warp; h < NC; h += NW) {
       if (!cols[h].active) continue;
+      const uint64_t* lb = reinterpret_cast<const uint64_t*>(scratch + v0);
       uint64_t a[KE];
 #pragma unroll
-      for (int e = 0; e < KE; ++e) a[e] = run[h * KP + e * 32 + lane];
-      for (int s = 0; s < s1 - s0; ++s) {
+      for (int e = 0; e < KE; ++e) a[e] = lb[h * KP + e * 32 + lane];
+      for (int s = 1; s < nsplit; ++s) {
         uint64_t bb[KE];
 #pragma unroll
-        for (int e = 0; e < KE; ++e) bb[e] = lbuf[(size_t)s * per_split + h * KP + e * 32 + lane];
+        for (int e = 0; e < KE; ++e) bb[e] = lb[(size_t)s * per_split + h * KP + e * 32 + lane];
         warp_merge_desc<KE>(a, bb, lane);
       }
 #pragma unroll
       for (int e = 0; e < KE; ++e) run[h * KP + e * 32 + lane] = a[e];
     }
     __syncthreads();
+  } else {
+    int chunk = (scratch_bytes - v0) / (per_split * 8);
+    if (chunk < 1) chunk = 1;
+    uint64_t* lbuf = reinterpret_cast<uint64_t*>(scratch + v0);
+    __syncthreads();
+    for (int s0 = 0; s0 < nsplit; s0 += chunk) {
+      const int s1 = s0 + chunk < nsplit ? s0 + chunk : nsplit;
+      const unsigned long long* src = G.lists + ((size_t)unit * G.nsplit_max + s0) * per_split;
+      const int total = (s1 - s0) * per_split;
+      for (int i = tid; i < total; i += blockDim.x) lbuf[i] = __ldcg(src + i);
+      __syncthreads();
+      for (int h = warp; h < NC; h += NW) {
+        if (!cols[h].active) continue;
+        uint64_t a[KE];
+#pragma unroll
+        for (int e = 0; e < KE; ++e) a[e] = run[h * KP + e * 32 + lane];
+        for (int s = 0; s < s1 - s0; ++s) {
+          uint64_t bb[KE];
+#pragma unroll
+          for (int e = 0; e < KE; ++e) bb[e] = lbuf[(size_t)s * per_split + h * KP + e * 32 + lane];
+          warp_merge_desc<KE>(a, bb, lane);
+        }
+#pragma unroll
+        for (int e = 0; e < KE; ++e) run[h * KP + e * 32 + lane] = a[e];
+      }
+      __syncthreads();
+    }
   }
 
-  // per column: C_i, the k-th key, the softmax over C_i
-  int* topj_all = reinterpret_cast<int*>(scratch);
-  float* wsm_all = reinterpret_cast<float*>(scratch + NC * KP * 4);
-  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
-  const long long cmax = 1 + (long long)G.W + kk;
-  int* tcount = reinterpret_cast<int*>(scratch + NC * KP * 4 + NW * 2048);  // [NC]
   // per column: the k-th key, the selected positions (ascending) and C_i
   for (int h = warp; h < NC; h += NW) {
     if (!cols[h].active) continue;
@@ -650,80 +729,19 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   if (!(G.flags & kDoPV)) return;
   __syncthreads();
 
-  // Stage every K and V row the softmax needs in shared memory with one burst
-  // of bulk copies: the band covering all windows of the block (and the
-  // anchor), then each column's top-k rows.
-  using S = Shape<BF16, D>;
-  long long plo = 0x7fffffffffffffffLL, phi = -1;
-  for (int h = 0; h < NC; ++h)
-    if (cols[h].active) {
-      plo = cols[h].pos < plo ? cols[h].pos : plo;
-      phi = cols[h].pos > phi ? cols[h].pos : phi;
-    }
-  const long long band_lo = plo - G.W + 1 > 0 ? plo - G.W + 1 : 0;
-  const long long nb = phi - band_lo + 1;
-  const long long anchor_slot = band_lo == 0 ? 0 : nb;
-  const long long top0 = nb + 1;
-  const long long nslots = top0 + (long long)NC * kk;
-  const int stage_off = (NC * KP * 4 + NW * 2048 + NC * 4 + 64 + 1023) & ~1023;
-  uint64_t* sbar = reinterpret_cast<uint64_t*>(scratch + stage_off - 64);
-  uint8_t* stage = scratch + stage_off;
-  const bool staged = phi >= 0 && (long long)stage_off + nslots * 2 * S::ROWB <= scratch_bytes;
-  bool ok = true;
-  if (staged) {
-    long long filled = nb + (band_lo == 0 ? 0 : 1);
-    for (int h = 0; h < NC; ++h)
-      if (cols[h].active) filled += tcount[h];
-    if (tid == 0) {
-      mbar_init(sbar, 1);
-      fence_mbar_init();
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (tid == 0) mbar_arrive_expect_tx(sbar, (uint32_t)(filled * 2 * S::ROWB));
-    const uint8_t* kb = reinterpret_cast<const uint8_t*>(G.kp);
-    const uint8_t* vb = reinterpret_cast<const uint8_t*>(G.vp);
-    for (long long sl = tid; sl < nslots; sl += blockDim.x) {
-      long long row = -1;
-      if (sl < nb) {
-        row = band_lo + sl;
-      } else if (sl == nb) {
-        row = band_lo == 0 ? -1 : 0;
-      } else {
-        const int h = (int)((sl - top0) / kk), i = (int)((sl - top0) % kk);
-        if (cols[h].active && i < tcount[h]) row = topj_all[h * KP + i];
-      }
-      if (row < 0) continue;
-      uint8_t* dst = stage + (size_t)sl * 2 * S::ROWB;
-      bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, sbar);
-      bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, sbar);
-    }
-    ok = mbar_wait(sbar, 0);
-    if (!ok && tid == 0) set_status(G.status, kStatusTimeout);
-    __syncthreads();
-  }
-
-  // per column: the softmax over C_i and the weighted sum of V
-  for (int h = warp; h < NC; h += NW) {
-    if (!cols[h].active || !ok) continue;
-    const int t = tcount[h];
-    const int* topj = topj_all + h * KP;
-    const long long p = cols[h].pos;
-    const bool wide = p - G.W + 1 <= 0;
-    const long long mEnt = wide ? p + 1 : 1 + t + G.W;
-    const long long wlo = p - G.W + 1;
-    float* wsm = wsm_all + warp * 512;
-    int* jsm = reinterpret_cast<int*>(wsm + 256);
-    if (staged) {
-      auto slot_of = [&](long long e) -> int {
-        if (wide) return (int)(e - band_lo);  // 0..p lies in the band, which starts at 0
-        if (e == 0) return (int)anchor_slot;
-        if (e <= t) return (int)(top0 + (long long)h * kk + (e - 1));
-        return (int)(wlo + (e - 1 - t) - band_lo);
-      };
-      warp_softmax_pv_staged<BF16, D, NC>(G, qd, h, mEnt, slot_of, stage, wsm, jsm,
-                                          G.out + cols[h].row * D, lane);
-    } else {
+  if (!fast) {
+    // one warp per column, rows from global memory
+    float* wsm_all = reinterpret_cast<float*>(scratch + v0);
+    for (int h = warp; h < NC; h += NW) {
+      if (!cols[h].active) continue;
+      const int t = tcount[h];
+      const int* topj = topj_all + h * KP;
+      const long long p = cols[h].pos;
+      const bool wide = p - G.W + 1 <= 0;
+      const long long mEnt = wide ? p + 1 : 1 + t + G.W;
+      const long long wlo = p - G.W + 1;
+      float* wsm = wsm_all + warp * 512;
+      int* jsm = reinterpret_cast<int*>(wsm + 256);
       auto entry = [&](long long e) -> long long {
         if (wide) return e;
         if (e == 0) return 0;
@@ -732,8 +750,104 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       };
       warp_softmax_pv<BF16, D, NC>(G, kvrow0, qd, h, mEnt, entry, wsm, jsm,
                                    G.out + cols[h].row * D, lane);
+      __syncwarp();
     }
-    __syncwarp();
+    return;
+  }
+
+  // the columns' top-k rows
+  {
+    long long tbytes = 0;
+    for (int h = 0; h < NC; ++h)
+      if (cols[h].active) tbytes += (long long)tcount[h] * 2 * S::ROWB;
+    if (tid == 0) mbar_arrive_expect_tx(&bars[2], (uint32_t)tbytes);
+    for (long long sl = tid; sl < (long long)NC * kk; sl += blockDim.x) {
+      const int h = (int)(sl / kk), i = (int)(sl % kk);
+      if (!cols[h].active || i >= tcount[h]) continue;
+      const long long row = topj_all[h * KP + i];
+      uint8_t* dst = stage + (size_t)(top0 + sl) * 2 * S::ROWB;
+      bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[2]);
+      bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[2]);
+    }
+    const bool ok = mbar_wait(&bars[1], 0) && mbar_wait(&bars[2], 0);
+    if (!ok && tid == 0) set_status(G.status, kStatusTimeout);
+    if (__syncthreads_or(!ok)) return;
+  }
+
+  // per-column constants, once: entries m, top-k count t, window start
+  int* cm = reinterpret_cast<int*>(scratch + off_lw + NC * mmax * 4);   // [NC] entries
+  int* slot_tab = reinterpret_cast<int*>(stage + nslots * 2 * S::ROWB);  // [NC][mmax]
+  if (tid < NC) {
+    const int h = tid;
+    const long long p = cols[h].pos;
+    cm[h] = !cols[h].active ? 0 : (int)(p - G.W + 1 <= 0 ? p + 1 : 1 + tcount[h] + G.W);
+  }
+  __syncthreads();
+  const float scale = G.scale;
+  const long long W = G.W;
+  // logits of every (column, entry), all threads; the entry's staged slot is
+  // kept for the weighted sum
+  for (long long i = tid; i < (long long)NC * mmax; i += blockDim.x) {
+    const int h = (int)(i / mmax);
+    const int e = (int)(i % mmax);
+    if (e >= cm[h]) continue;
+    const long long p = cols[h].pos;
+    const int t = tcount[h];
+    long long sl;
+    if (p - W + 1 <= 0) sl = e - band_lo;  // 0..p lies in the band, which starts at 0
+    else if (e == 0) sl = anchor_slot;
+    else if (e <= t) sl = top0 + (long long)h * kk + (e - 1);
+    else sl = (p - W + 1) + (e - 1 - t) - band_lo;
+    slot_tab[i] = (int)sl;
+    lw[i] = scale * score_row_smem<BF16, D, NC>(stage + (size_t)sl * 2 * S::ROWB, qd, h);
+  }
+  __syncthreads();
+  // per column: max, weights, normaliser
+  for (int h = warp; h < NC; h += NW) {
+    const int m = cm[h];
+    if (m == 0) continue;
+    float* l = lw + (size_t)h * mmax;
+    float mx = -INFINITY;
+    for (int e = lane; e < m; e += 32) mx = fmaxf(mx, l[e]);
+    mx = warp_max(mx);
+    float zs = 0.f;
+    for (int e = lane; e < m; e += 32) {
+      const float w = expf(l[e] - mx);
+      l[e] = w;
+      zs += w;
+    }
+    zs = warp_sum(zs);
+    if (lane == 0) zsum[h] = zs;
+  }
+  __syncthreads();
+  // out[h][c..c+1] = sum_e w_e v_e[c..c+1] / Z, one thread per (column, element pair)
+  for (int i = tid; i < NC * (D / 2); i += blockDim.x) {
+    const int h = i / (D / 2), c = 2 * (i % (D / 2));
+    const int m = cm[h];
+    if (m == 0) continue;
+    const float* w = lw + (size_t)h * mmax;
+    const int* st = slot_tab + (size_t)h * mmax;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+    for (int e = 0; e < m; ++e) {
+      const uint8_t* vr = stage + (size_t)st[e] * 2 * S::ROWB + S::ROWB;
+      float v0, v1;
+      if constexpr (BF16) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(vr + c * 2);
+        v0 = __uint_as_float(u << 16);
+        v1 = __uint_as_float(u & 0xffff0000u);
+      } else {
+        const float2 f = *reinterpret_cast<const float2*>(vr + c * 4);
+        v0 = f.x;
+        v1 = f.y;
+      }
+      a0 = fmaf(w[e], v0, a0);
+      a1 = fmaf(w[e], v1, a1);
+    }
+    const float z = zsum[h];
+    float* o = G.out + cols[h].row * D + c;
+    o[0] = z > 0.f ? a0 / z : 0.f;
+    o[1] = z > 0.f ? a1 / z : 0.f;
   }
 }
 

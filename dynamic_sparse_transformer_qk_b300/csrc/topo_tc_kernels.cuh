@@ -407,12 +407,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
     for (int h = 0; h < NC; ++h) {
       uint64_t* hb = mybuf + h * CAP;
-      const TcKept kept = tc_compact<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
+      // A buffer of at most 64 entries sorts in half the network; that
+      // rewrites (and zero-fills) only slots 0..63, so it is used only when
+      // the survivor list read below is 64 entries long (LL == 64).
+      TcKept kept;
+      if (LL == 64 && cnt[h] <= 64)
+        kept = tc_compact<2>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
+      else
+        kept = tc_compact<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
       if (kept.keep > LL) ovf[h] = true;
       if (lane == 0) {
         meta[e * NC + h].delta = coef[h] * kmag;
         meta[e * NC + h].overflow = ovf[h] ? 1 : 0;
       }
+      // the survivors' K rows on their way to L2 for the exact rescoring
+      for (int i = lane; i < kept.keep && i < LL; i += 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(
+            reinterpret_cast<const uint8_t*>(G.kp) + (kvrow0 + key_pos(hb[i])) * S::ROWB));
     }
   }
   // every role is done with the ring and the accumulators
@@ -489,6 +500,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int ee = 0; ee < KE; ++ee) {
       const int i = ee * 32 + lane;
       dst[i] = (i < kk && cols[h].active) ? x[ee] : 0ull;
+      // the V rows the final softmax may gather, on their way to L2
+      if (i < kk && cols[h].active && x[ee] != 0ull && G.vp)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(
+            reinterpret_cast<const uint8_t*>(G.vp) + (kvrow0 + key_pos(x[ee])) * S::ROWB));
     }
   }
   if (!finish_split(G.counters + unit, nsplit, misc)) return;
