@@ -52,6 +52,25 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
+def rank_workload(w: synth.Workload, rank: int) -> synth.Workload:
+    """Each rank serves its own sequences: same shapes, its own seeds (weak
+    scaling; no data-path collective)."""
+    return w.with_(seed=w.seed + 7919 * rank) if rank else w
+
+
+def job_rate(ms_local: float, queries_per_rank: int, world: int):
+    """Whole-job time (max over ranks, gloo all-reduce on the host) and rate:
+    queries of all ranks / that time."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        tt = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return ms, queries_per_rank * world / (ms / 1000.0)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -247,8 +266,7 @@ def bench_ours(args, w: synth.Workload):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     # every rank serves its own sequences (weak scaling, no data-path collective)
-    wr = w.with_(seed=w.seed + 7919 * rank) if rank else w
-    x = synth.make(wr)
+    x = synth.make(rank_workload(w, rank))
 
     def to_dev(a):
         t = torch.from_numpy(a)
@@ -297,13 +315,8 @@ def bench_ours(args, w: synth.Workload):
                 graph.replay()
             torch.cuda.synchronize()
     per = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(per) / len(per)
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms, value = job_rate(sum(per) / len(per), w.B, world)
     queries = w.B * world
-    value = queries / (ms / 1000.0)
 
     # dominant kernel roofline: the fused select kernel streams K once and
     # gathers the 1+W+k V rows (and the anchor/window K rows) per query head
@@ -357,11 +370,7 @@ def bench_ours(args, w: synth.Workload):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ems = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ems], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ems = float(tt.item())
+    ems, _ = job_rate(e0.elapsed_time(e1) / args.steps, w.B, world)
     h2d = hq.numel() * hq.element_size() + 2 * hk_row.numel() * hk_row.element_size()
     d2h = hout.numel() * hout.element_size()
     e2e = {"value": queries / (ems / 1000.0), "unit": "queries/s", "h2d_bytes_per_step": h2d,
@@ -539,6 +548,57 @@ def bench_prefill(args, w: synth.Workload):
     print(json.dumps(line), flush=True)
 
 
+def eps_report(args):
+    """The pages' exactness argument rests on the dense-softmax mass left out of
+    C_i being below the float32 ULP.  Per workload: that excluded mass eps
+    (GPU, every row; sampled rows for the 64K prefill), and on oracle-sampled
+    rows the largest excluded weight against 2^-23 and the anchor's weight."""
+    import torch
+    import oracle
+    import dynamic_sparse_transformer_qk_b300 as topo
+    rng = np.random.default_rng(20260211)
+    cases = [(i, synth.CONFIGS[i]) for i in (0, 1, 2, 4)]
+    cases += [(3, synth.CONFIGS[3].with_(W=W)) for W in synth.PREFILL_WINDOWS]
+    for cid, w in cases:
+        x = synth.make(w)
+
+        def dev(a):
+            t = torch.from_numpy(a)
+            return (t.view(torch.bfloat16) if w.dtype == "bf16" else t).cuda()
+
+        q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+        nrows = w.B * w.Hq * w.nq
+        if cid == 3:
+            # last chunk of the chunked prefill (rows 61,440..65,535)
+            c = w.n // w.chunk - 1
+            qc = q[:, :, c * w.chunk:].contiguous()
+            _, _, excl = topo.forward(qc, k, v, W=w.W, topk=w.k, n=w.n, scale=w.scale,
+                                      want_excl=True)
+            flat = np.arange(nrows).reshape(w.B, w.Hq, w.nq)[:, :, c * w.chunk:].reshape(-1)
+            gexcl = excl.cpu().numpy().reshape(-1).astype(np.float64)
+            sample = np.sort(rng.choice(flat, size=64, replace=False))
+        else:
+            _, _, excl = topo.forward(q, k, v, W=w.W, topk=w.k, n=w.n, scale=w.scale,
+                                      want_excl=True)
+            gexcl = excl.cpu().numpy().reshape(-1).astype(np.float64)
+            sample = np.sort(rng.choice(nrows, size=min(nrows, 256), replace=False))
+        torch.cuda.synchronize()
+        P = oracle.make_params(w.B, w.Hq, w.Hkv, w.d, w.n, w.nq, w.W, w.k, w.scale, w.dtype)
+        o = oracle.topo_attn(P, x["q"], x["k"], x["v"], rows=sample, want=("excl", "wmax", "p0"))
+        ulp, half = 2.0 ** -23, 2.0 ** -24
+        line = {
+            "workload": workload_desc(w), "rows": int(gexcl.size),
+            "eps_median": float(np.median(gexcl)), "eps_max": float(gexcl.max()),
+            "eps_below_half_ulp_frac": float((gexcl < half).mean()),
+            "oracle_rows": int(sample.size),
+            "wmax_over_ulp_median": float(np.median(o["wmax"] / ulp)),
+            "wmax_over_ulp_max": float(o["wmax"].max() / ulp),
+            "wmax_below_ulp_frac": float((o["wmax"] < ulp).mean()),
+            "anchor_weight_median": float(np.median(o["p0"])),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -553,11 +613,16 @@ def main():
                     help="override the causal length (profiling runs on smaller caches)")
     ap.add_argument("--profile", action="store_true",
                     help="time the steps only: no e2e, dense, clock padding or CPU baseline")
+    ap.add_argument("--eps-report", action="store_true",
+                    help="report the excluded softmax mass against the float32 ULP per workload")
     ap.add_argument("--window", type=int, default=0,
                     help="window W of the prefill workload (256, 128 or 64; default 256)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.eps_report:
+        eps_report(args)
+        return
     w = synth.CONFIGS[WORKLOADS[args.workload]]
     if args.n:
         w = w.with_(n=args.n, name=f"{w.name} (n overridden to {args.n})")
