@@ -22,9 +22,9 @@
 //                            thread owns one column: it keeps a candidate
 //                            buffer in shared memory, appends every score
 //                            above the column's cut and, when a buffer fills,
-//                            the warp compacts its 32 columns one at a time
-//                            (bitonic sort across the warp): the cut becomes
-//                            T - 2 delta, T the column's k-th best tensor-core
+//                            the warp compacts that column (a bisection on
+//                            warp-wide counts): the cut becomes T - 2 delta,
+//                            T at most the column's k-th best tensor-core
 //                            score and delta the bound on |tensor core - exact
 //                            chain| (see topo_tc_kernels.cuh).  Survivors go to
 //                            the workspace;
@@ -46,10 +46,10 @@ namespace topo {
 
 constexpr int kPfCols = 128;   // query columns per work item (MMA M)
 constexpr int kPfKeys = 128;   // keys per tile (MMA N)
-constexpr int kPfCap = 64;     // candidate slots per column
+constexpr int kPfCap = 96;     // candidate slots per column
 constexpr int kPfSub = 8;      // scores offered between room checks
 constexpr int kPfLL = 64;      // survivors published per column
-constexpr int kPfStride = kPfCols + 1;  // buffer row stride (words): conflict-free both ways
+constexpr int kPfStride = kPfCols + 1;  // buffer row stride (entries)
 constexpr int kPfEpiWarps = 4; // one per TMEM lane quarter
 constexpr int kPfWarps = 2 + kPfEpiWarps;  // + TMA producer + MMA issuer
 constexpr int kPfThreads = 32 * kPfWarps;
@@ -62,7 +62,7 @@ struct PfSmem {
     int o = 0;
     ring = o;   o += stages * tile;               // multiple of 1024
     qtile = o;  o += kPfCols * D * 2;             // A operand (1024-aligned)
-    buf = o;    o += 2 * kPfCap * kPfStride * 4;  // scores, then positions [slot][column]
+    buf = o;    o += kPfCap * kPfStride * 8;      // (score, position) entries [slot][column]
     bars = o;   o += (2 * stages + 4) * 8;        // full, empty, acc_full[2], acc_empty[2]
     misc = o;   o += 64;
     total = o + 1024;
@@ -117,49 +117,65 @@ __device__ __forceinline__ float max8(const float* v) {
   return fmaxf(max3f(v[0], v[1], v[2]), max3f(v[3], v[4], max3f(v[5], v[6], v[7])));
 }
 
-// Compact the buffer of column c of this warp: T = its k-th best score (the
-// slots sorted across the warp; -inf while it has fewer than k entries), keep
-// the entries with score >= T - 2 delta (in any order) and update lane c's
-// count and cut.  `final` never flags overflow.
-static __device__ __noinline__ PfState pf_compact(float* bs, int* bj, int quarter, int lane,
-                                                  int kk, int c, float two_delta, PfState st,
+// Compact the buffer of column c of this warp.  A bisection on warp-wide
+// counts finds U with at least k buffered scores >= U (so U is at most the
+// k-th best, within 1/1024 of the buffered range); entries with score >=
+// U - 2 delta are kept (in any order) and lane c's count and cut are updated.
+// While the column has fewer than k entries everything is kept.  `final`
+// never flags overflow.  An entry is (score, position bits).
+static __device__ __noinline__ PfState pf_compact(float2* be, int quarter, int lane, int kk,
+                                                  int c, float two_delta, PfState st,
                                                   bool final) {
+  constexpr int R = (kPfCap + 31) / 32;
   const int cc = quarter * 32 + c;
   const int cnt_c = __shfl_sync(kFull, st.cnt, c);
   const float td = __shfl_sync(kFull, two_delta, c);
-  const bool h0 = lane < cnt_c, h1 = lane + 32 < cnt_c;
-  const float v0 = h0 ? bs[lane * kPfStride + cc] : -INFINITY;
-  const float v1 = h1 ? bs[(lane + 32) * kPfStride + cc] : -INFINITY;
-  const int j0 = h0 ? bj[lane * kPfStride + cc] : 0;
-  const int j1 = h1 ? bj[(lane + 32) * kPfStride + cc] : 0;
-  float T = -INFINITY;
+  float2 e[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int slot = lane + 32 * r;
+    e[r] = slot < cnt_c ? be[slot * kPfStride + cc] : make_float2(-INFINITY, 0.f);
+  }
+  float cut = -INFINITY;
   if (kk > 0 && cnt_c >= kk) {
-    float x[2] = {v0, v1};
-    warp_sort_desc_f32<2>(x, lane);
-    const int i = kk - 1;
-    T = __shfl_sync(kFull, (i >> 5) ? x[1] : x[0], i & 31);
+    float hi = -INFINITY, lo = INFINITY;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      hi = fmaxf(hi, e[r].x);
+      lo = fminf(lo, e[r].x == -INFINITY ? INFINITY : e[r].x);
+    }
+    hi = warp_max(hi);
+    lo = -warp_max(-lo);  // at least k entries are >= lo
+#pragma unroll 1
+    for (int it = 0; it < 10; ++it) {
+      const float mid = 0.5f * (lo + hi);
+      int n = 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r) n += __popc(__ballot_sync(kFull, e[r].x >= mid));
+      if (n >= kk) lo = mid;
+      else hi = mid;
+    }
+    cut = lo - td;
   }
-  const float cut = T - td;
-  const bool k0 = h0 && (T == -INFINITY || v0 >= cut);
-  const bool k1 = h1 && (T == -INFINITY || v1 >= cut);
-  const unsigned b0 = __ballot_sync(kFull, k0), b1 = __ballot_sync(kFull, k1);
-  const unsigned below = (1u << lane) - 1u;
-  const int keep = __popc(b0) + __popc(b1);
+  unsigned b[R];
+  int keep = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    b[r] = __ballot_sync(kFull, e[r].x != -INFINITY && e[r].x >= cut);
+    keep += __popc(b[r]);
+  }
   __syncwarp();
-  if (k0) {
-    const int p = __popc(b0 & below);
-    bs[p * kPfStride + cc] = v0;
-    bj[p * kPfStride + cc] = j0;
-  }
-  if (k1) {
-    const int p = __popc(b0) + __popc(b1 & below);
-    bs[p * kPfStride + cc] = v1;
-    bj[p * kPfStride + cc] = j1;
+  const unsigned below = (1u << lane) - 1u;
+  int base = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (b[r] & (1u << lane)) be[(base + __popc(b[r] & below)) * kPfStride + cc] = e[r];
+    base += __popc(b[r]);
   }
   __syncwarp();
   if (lane == c) {
     st.cnt = keep;
-    st.thr = T == -INFINITY ? -INFINITY : cut;
+    st.thr = cut;
     if (!final && keep + kPfSub > kPfCap) {  // the buffer is full of near ties
       st.ovf = 1;
       st.thr = INFINITY;
@@ -171,11 +187,12 @@ static __device__ __noinline__ PfState pf_compact(float* bs, int* bj, int quarte
 // Offer 64 consecutive scores (positions jg..jg+63) of this thread's column:
 // the maxima of the eight 8-score groups first (independent), one warp
 // reduction, and the append path only for the groups where some column has a
-// candidate.
+// candidate.  The append writes every score of the group to the next free
+// slot and advances the count only past the ones above the cut (no branch,
+// one 64-bit store per score); the room check keeps 8 slots free.
 __device__ __forceinline__ void pf_offer64(const float (&sa)[32], const float (&sb)[32],
-                                           long long jg, float* bs, int* bj, int quarter,
-                                           int lane, int cl, int kk, float two_delta,
-                                           PfState& st) {
+                                           long long jg, float2* be, int quarter, int lane,
+                                           int cl, int kk, float two_delta, PfState& st) {
   float m[8];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
@@ -194,17 +211,17 @@ __device__ __forceinline__ void pf_offer64(const float (&sa)[32], const float (&
     while (full) {
       const int c = __ffs(full) - 1;
       full &= full - 1;
-      st = pf_compact(bs, bj, quarter, lane, kk, c, two_delta, st, false);
+      st = pf_compact(be, quarter, lane, kk, c, two_delta, st, false);
     }
     const float* v = s < 4 ? sa + 8 * s : sb + 8 * (s - 4);
+    const int j0 = (int)(jg + 8 * s);
+    int n = st.ovf ? 0 : st.cnt;  // an overflowed column only scribbles on its slot 0
 #pragma unroll
     for (int i = 0; i < kPfSub; ++i) {
-      if (v[i] > st.thr) {
-        bs[st.cnt * kPfStride + cl] = v[i];
-        bj[st.cnt * kPfStride + cl] = (int)(jg + 8 * s + i);
-        ++st.cnt;
-      }
+      be[n * kPfStride + cl] = make_float2(v[i], __int_as_float(j0 + i));
+      n += v[i] > st.thr ? 1 : 0;
     }
+    if (!st.ovf) st.cnt = n;
   }
 }
 
@@ -222,8 +239,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const PfSmem L(D, stages);
   uint8_t* ring = sm + L.ring;
   uint8_t* qtile = sm + L.qtile;
-  float* bs = reinterpret_cast<float*>(sm + L.buf);
-  int* bj = reinterpret_cast<int*>(sm + L.buf + kPfCap * kPfStride * 4);
+  float2* be = reinterpret_cast<float2*>(sm + L.buf);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + stages;
   uint64_t* accf = empty + stages;
@@ -395,13 +411,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               if (jg + 32 + i > jhi) sb[i] = -INFINITY;
             }
           }
-          pf_offer64(sa, sb, jg, bs, bj, quarter, lane, cl, kk, two_delta, st);
+          pf_offer64(sa, sb, jg, be, quarter, lane, cl, kk, two_delta, st);
         }
       }
       // survivors of each column (any order) to the workspace
 #pragma unroll 1
       for (int c = 0; c < 32; ++c)
-        st = pf_compact(bs, bj, quarter, lane, kk, c, two_delta, st, true);
+        st = pf_compact(be, quarter, lane, kk, c, two_delta, st, true);
 #pragma unroll 1
       for (int c = 0; c < 32; ++c) {
         const int cc = quarter * 32 + c;
@@ -414,7 +430,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int r = 0; r < kPfLL / 32; ++r) {
           const int ee = lane + 32 * r;
-          dst[ee] = ee < cnt_c ? (uint32_t)(bj[ee * kPfStride + cc] - 1) : 0u;
+          dst[ee] = ee < cnt_c ? (uint32_t)(__float_as_int(be[ee * kPfStride + cc].y) - 1) : 0u;
         }
         if (lane == 0) G.surv_cnt[gcol] = ovl ? -1 : cnt_c;
       }
