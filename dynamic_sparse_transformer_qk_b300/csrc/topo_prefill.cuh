@@ -15,7 +15,9 @@
 //                            (the scale of the tensor-core rounding bound);
 //   prefill_scan_kernel      persistent; one work item = 128 query columns
 //                            (query row x head pairs of one KV head) against
-//                            all their candidate keys, 128 keys per tile:
+//                            all their candidate keys, 128 keys per tile, in
+//                            two passes over the same tiles (pass 1 finds
+//                            each column's starting cut from tile maxima):
 //                            M = 128 columns (A: queries, resident in shared
 //                            memory), N = 128 keys (B: K tile by TMA), the
 //                            accumulator in TMEM (two buffers).  Each epilogue
@@ -175,13 +177,64 @@ static __device__ __noinline__ PfState pf_compact(float2* be, int quarter, int l
   __syncwarp();
   if (lane == c) {
     st.cnt = keep;
-    st.thr = cut;
+    st.thr = fmaxf(st.thr, cut);
     if (!final && keep + kPfSub > kPfCap) {  // the buffer is full of near ties
       st.ovf = 1;
       st.thr = INFINITY;
     }
   }
   return st;
+}
+
+// Compact this thread's own column (every lane of the warp at once, no
+// cross-lane work): the same bisection as pf_compact on per-lane counts,
+// entries >= U - 2 delta kept in place, the cut never lowered.  Columns with
+// fewer than max(k, at_least) entries, or already overflowed, are left as
+// they are.  A column left with fewer than `room` free slots overflows; with
+// `hold` its cut stays finite (appends stop), else the cut becomes +inf.
+static __device__ __noinline__ PfState pf_compact_lane(float2* be, int cl, int kk, float two_delta,
+                                                       PfState st, int at_least, int room,
+                                                       bool hold) {
+  const int n = st.cnt;
+  if (st.ovf || kk <= 0 || n < kk || n < at_least) return st;
+  float lo = INFINITY, hi = -INFINITY;
+  for (int i = 0; i < n; ++i) {
+    const float v = be[i * kPfStride + cl].x;
+    lo = fminf(lo, v);
+    hi = fmaxf(hi, v);
+  }
+#pragma unroll 1
+  for (int it = 0; it < 10; ++it) {
+    const float mid = 0.5f * (lo + hi);
+    int c = 0;
+    for (int i = 0; i < n; ++i) c += be[i * kPfStride + cl].x >= mid ? 1 : 0;
+    if (c >= kk) lo = mid;
+    else hi = mid;
+  }
+  const float cut = lo - two_delta;
+  int w = 0;
+  for (int i = 0; i < n; ++i) {  // in place: the write slot never passes the read slot
+    const float2 e = be[i * kPfStride + cl];
+    be[w * kPfStride + cl] = e;
+    w += e.x >= cut ? 1 : 0;
+  }
+  st.cnt = w;
+  st.thr = fmaxf(st.thr, cut);
+  if (w + room > kPfCap) {
+    st.ovf = 1;
+    if (!hold) st.thr = INFINITY;
+  }
+  return st;
+}
+
+__device__ __forceinline__ float max64(const float (&a)[32], const float (&b)[32]) {
+  float m[8];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    m[s] = max8(a + 8 * s);
+    m[4 + s] = max8(b + 8 * s);
+  }
+  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 // Offer 64 consecutive scores (positions jg..jg+63) of this thread's column:
@@ -308,7 +361,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // ---------------- TMA producer ----------------------------------------
       if (lane == 0) {
         if (ntiles > 0) prefetch_tmap(&map_k);
-        for (int t = 0; t < ntiles; ++t) {
+        for (int t = 0; t < 2 * ntiles; ++t) {
           if (misc[0]) break;
           const long long gs = seq + t;
           const int s = (int)(gs % stages);
@@ -320,7 +373,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           uint8_t* dst = ring + (size_t)s * TILEB;
           mbar_arrive_expect_tx(&full[s], (uint32_t)TILEB);
-          const int y = (int)(kvrow0 + 1 + (long long)t * kPfKeys);
+          const int tt = t < ntiles ? t : t - ntiles;  // both passes run the same tiles
+          const int y = (int)(kvrow0 + 1 + (long long)tt * kPfKeys);
 #pragma unroll
           for (int cc = 0; cc < S::NCH; ++cc)
             tma_load_2d(dst + cc * (kPfKeys * 128), &map_k, cc * S::EPC, y, &full[s]);
@@ -331,7 +385,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (lane == 0) {
         constexpr uint32_t idesc = tc::idesc_bf16_f32(kPfCols, kPfKeys);
         const uint32_t qaddr = smem_addr(qtile);
-        for (int t = 0; t < ntiles; ++t) {
+        for (int t = 0; t < 2 * ntiles; ++t) {
           if (misc[0]) break;
           const long long gs = seq + t;
           const int s = (int)(gs % stages);
@@ -377,7 +431,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float two_delta = 2.f * tc_delta_factor(D) * qn1 * 1.001f * kmx;
       PfState st{0, -INFINITY, 0};
       const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
-      for (int t = 0; t < ntiles; ++t) {
+      // Pass 1 (t < ntiles) offers only the largest score of each tile (one
+      // value per 128 keys); the k-th largest such maximum U is a lower bound
+      // of the column's k-th best tensor-core score (k distinct keys reach
+      // it), so U - 2 delta is a valid starting cut for pass 2, which offers
+      // every score of the same tiles.  Both passes compute the same scores
+      // (identical operands and instruction sequence).
+      for (int t = 0; t < 2 * ntiles; ++t) {
+        const bool p1 = t < ntiles;
+        if (t == ntiles) {
+          st = pf_compact_lane(be, cl, kk, two_delta, st, 0, 0, true);
+          st.cnt = 0;
+          st.ovf = 0;
+        }
         const long long gs = seq + t;
         const int ab = (int)(gs & 1);
         const uint32_t around = (uint32_t)(gs >> 1);
@@ -390,34 +456,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const long long j0 = 1 + (long long)t * kPfKeys;
-#pragma unroll 1
-        for (int half = 0; half < kPfKeys / 64; ++half) {
-          float sa[32], sb[32];
-          const uint32_t ta = tq + (uint32_t)(ab * kPfKeys + half * 64);
+        const int tt = p1 ? t : t - ntiles;
+        const long long j0 = 1 + (long long)tt * kPfKeys;
+        // the whole tile (128 scores of this column) in registers, then the
+        // accumulator goes straight back to the MMA issuer
+        float sa[32], sb[32], sc[32], sd[32];
+        {
+          const uint32_t ta = tq + (uint32_t)(ab * kPfKeys);
           tc::tmem_ld32(ta, sa);
           tc::tmem_ld32(ta + 32, sb);
+          tc::tmem_ld32(ta + 64, sc);
+          tc::tmem_ld32(ta + 96, sd);
           tc::tmem_ld_wait();
-          if (half == kPfKeys / 64 - 1) {  // this warp is done with the accumulator
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acce[ab]);
-          }
-          const long long jg = j0 + half * 64;
-          if (jg + 63 > jhi) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[ab]);
+        }
+        if (j0 + kPfKeys - 1 > jhi) {  // keys past the column's last candidate
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (jg + i > jhi) sa[i] = -INFINITY;
-              if (jg + 32 + i > jhi) sb[i] = -INFINITY;
-            }
+          for (int i = 0; i < 32; ++i) {
+            if (j0 + i > jhi) sa[i] = -INFINITY;
+            if (j0 + 32 + i > jhi) sb[i] = -INFINITY;
+            if (j0 + 64 + i > jhi) sc[i] = -INFINITY;
+            if (j0 + 96 + i > jhi) sd[i] = -INFINITY;
           }
-          pf_offer64(sa, sb, jg, be, quarter, lane, cl, kk, two_delta, st);
+        }
+        if (p1) {
+          const float bm = fmaxf(max64(sa, sb), max64(sc, sd));
+          if (__any_sync(kFull, !st.ovf && st.cnt >= kPfCap))
+            st = pf_compact_lane(be, cl, kk, two_delta, st, 0, 1, true);
+          if (!st.ovf && bm > st.thr) {
+            be[st.cnt * kPfStride + cl] = make_float2(bm, __int_as_float(tt));
+            ++st.cnt;
+          }
+        } else {
+          pf_offer64(sa, sb, j0, be, quarter, lane, cl, kk, two_delta, st);
+          pf_offer64(sc, sd, j0 + 64, be, quarter, lane, cl, kk, two_delta, st);
         }
       }
       // survivors of each column (any order) to the workspace
-#pragma unroll 1
-      for (int c = 0; c < 32; ++c)
-        st = pf_compact(be, quarter, lane, kk, c, two_delta, st, true);
+      if (__any_sync(kFull, !st.ovf && st.cnt > kPfLL))
+        st = pf_compact_lane(be, cl, kk, two_delta, st, kPfLL + 1, 0, false);
 #pragma unroll 1
       for (int c = 0; c < 32; ++c) {
         const int cc = quarter * 32 + c;
@@ -435,7 +514,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) G.surv_cnt[gcol] = ovl ? -1 : cnt_c;
       }
     }
-    seq += ntiles;
+    seq += 2 * ntiles;
   }
 
   // no copy into shared memory and no MMA may outlive the CTA
