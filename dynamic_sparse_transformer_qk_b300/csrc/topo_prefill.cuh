@@ -361,11 +361,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // ---------------- TMA producer ----------------------------------------
       if (lane == 0) {
         if (ntiles > 0) prefetch_tmap(&map_k);
-        for (int t = 0; t < 2 * ntiles; ++t) {
+        // ring slot and round of tile seq + t, advanced without a division per tile
+        int s = (int)(seq % stages);
+        uint32_t round = (uint32_t)(seq / stages);
+        for (int t = 0; t < 2 * ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
+                 round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
-          const long long gs = seq + t;
-          const int s = (int)(gs % stages);
-          const uint32_t round = (uint32_t)(gs / stages);
           if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
             set_status(G.status, kStatusTimeout);
             misc[0] = 1;
@@ -384,12 +385,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // ---------------- MMA issuer --------------------------------------------
       if (lane == 0) {
         constexpr uint32_t idesc = tc::idesc_bf16_f32(kPfCols, kPfKeys);
-        const uint32_t qaddr = smem_addr(qtile);
-        for (int t = 0; t < 2 * ntiles; ++t) {
+        // descriptors of the A operand and of ring slot 0; a 16-byte step of the
+        // start address is +1 in the descriptor's low field (addresses < 256 KB)
+        const uint64_t adesc = tc::smem_desc_sw128(smem_addr(qtile));
+        const uint64_t bdesc0 = tc::smem_desc_sw128(smem_addr(ring));
+        int s = (int)(seq % stages);
+        uint32_t round = (uint32_t)(seq / stages);
+        for (int t = 0; t < 2 * ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
+                 round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
           const long long gs = seq + t;
-          const int s = (int)(gs % stages);
-          const uint32_t round = (uint32_t)(gs / stages);
           const int ab = (int)(gs & 1);
           const uint32_t around = (uint32_t)(gs >> 1);
           if (!mbar_wait(&acce[ab], (around & 1u) ^ 1u) || !mbar_wait(&full[s], round & 1u)) {
@@ -398,12 +403,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             break;
           }
           tc::fence_after_sync();
-          const uint32_t kaddr = smem_addr(ring + (size_t)s * TILEB);
+          const uint64_t bdesc = bdesc0 + (uint64_t)((s * TILEB) >> 4);
+          const uint32_t dt = tmem + (uint32_t)(ab * kPfKeys);
 #pragma unroll
           for (int ks16 = 0; ks16 < KSTEPS; ++ks16) {
-            const uint32_t off = (ks16 >> 2) * (kPfCols * 128) + (ks16 & 3) * 32;
-            tc::mma_bf16(tmem + (uint32_t)(ab * kPfKeys), tc::smem_desc_sw128(qaddr + off),
-                         tc::smem_desc_sw128(kaddr + off), idesc, ks16 > 0);
+            const uint32_t off = ((ks16 >> 2) * (kPfCols * 128) + (ks16 & 3) * 32) >> 4;
+            tc::mma_bf16(dt, adesc + off, bdesc + off, idesc, ks16 > 0);
           }
           tc::mma_commit(&empty[s]);  // the K stage is free once these MMAs are done
           tc::mma_commit(&accf[ab]);
