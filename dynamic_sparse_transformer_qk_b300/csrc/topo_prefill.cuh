@@ -20,7 +20,7 @@
 //                            each column's starting cut from tile maxima):
 //                            M = 128 columns (A: queries, resident in shared
 //                            memory), N = 128 keys (B: K tile by TMA), the
-//                            accumulator in TMEM (two buffers).  Each epilogue
+//                            accumulator in TMEM (four buffers).  Each epilogue
 //                            thread owns one column: it keeps a candidate
 //                            buffer in shared memory, appends every score
 //                            above the column's cut and, when a buffer fills,
@@ -53,6 +53,7 @@ constexpr int kPfSub = 8;      // scores offered between room checks
 constexpr int kPfLL = 64;      // survivors published per column
 constexpr int kPfStride = kPfCols + 1;  // buffer row stride (entries)
 constexpr int kPfEpiWarps = 4; // one per TMEM lane quarter
+constexpr int kPfAcc = 4;      // TMEM accumulator buffers (128 columns each)
 constexpr int kPfWarps = 2 + kPfEpiWarps;  // + TMA producer + MMA issuer
 constexpr int kPfThreads = 32 * kPfWarps;
 
@@ -65,7 +66,7 @@ struct PfSmem {
     ring = o;   o += stages * tile;               // multiple of 1024
     qtile = o;  o += kPfCols * D * 2;             // A operand (1024-aligned)
     buf = o;    o += kPfCap * kPfStride * 8;      // (score, position) entries [slot][column]
-    bars = o;   o += (2 * stages + 4) * 8;        // full, empty, acc_full[2], acc_empty[2]
+    bars = o;   o += (2 * stages + 2 * kPfAcc) * 8;  // full, empty, acc_full[], acc_empty[]
     misc = o;   o += 64;
     total = o + 1024;
   }
@@ -237,21 +238,16 @@ __device__ __forceinline__ float max64(const float (&a)[32], const float (&b)[32
   return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
-// Offer 64 consecutive scores (positions jg..jg+63) of this thread's column:
-// the maxima of the eight 8-score groups first (independent), one warp
-// reduction, and the append path only for the groups where some column has a
+// Offer 64 consecutive scores (positions jg..jg+63) of this thread's column,
+// given the maxima m[0..7] of their eight 8-score groups: one warp reduction,
+// and the append path only for the groups where some column has a
 // candidate.  The append writes every score of the group to the next free
 // slot and advances the count only past the ones above the cut (no branch,
 // one 64-bit store per score); the room check keeps 8 slots free.
 __device__ __forceinline__ void pf_offer64(const float (&sa)[32], const float (&sb)[32],
-                                           long long jg, float2* be, int quarter, int lane,
-                                           int cl, int kk, float two_delta, PfState& st) {
-  float m[8];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    m[s] = max8(sa + 8 * s);
-    m[4 + s] = max8(sb + 8 * s);
-  }
+                                           const float* m, long long jg, float2* be,
+                                           int quarter, int lane, int cl, int kk,
+                                           float two_delta, PfState& st) {
   unsigned lm = 0u;
 #pragma unroll
   for (int s = 0; s < 8; ++s) lm |= (m[s] > st.thr) ? (1u << s) : 0u;
@@ -296,7 +292,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + stages;
   uint64_t* accf = empty + stages;
-  uint64_t* acce = accf + 2;
+  uint64_t* acce = accf + kPfAcc;
   volatile int* misc = reinterpret_cast<volatile int*>(sm + L.misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L.misc + 32);
 
@@ -306,14 +302,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kPfAcc; ++a) {
       mbar_init(&accf[a], 1);
       mbar_init(&acce[a], kPfEpiWarps);
     }
     fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tslot, 2 * kPfKeys);
+    tc::tmem_alloc(tslot, kPfAcc * kPfKeys);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -395,8 +391,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                  round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
           const long long gs = seq + t;
-          const int ab = (int)(gs & 1);
-          const uint32_t around = (uint32_t)(gs >> 1);
+          const int ab = (int)(gs & (kPfAcc - 1));
+          const uint32_t around = (uint32_t)(gs >> 2);
           if (!mbar_wait(&acce[ab], (around & 1u) ^ 1u) || !mbar_wait(&full[s], round & 1u)) {
             set_status(G.status, kStatusTimeout);
             misc[0] = 1;
@@ -450,8 +446,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           st.ovf = 0;
         }
         const long long gs = seq + t;
-        const int ab = (int)(gs & 1);
-        const uint32_t around = (uint32_t)(gs >> 1);
+        const int ab = (int)(gs & (kPfAcc - 1));
+        const uint32_t around = (uint32_t)(gs >> 2);
         const bool ok = __all_sync(kFull, mbar_wait(&accf[ab], around & 1u));
         if (!ok || misc[0]) {
           if (!ok && lane == 0) {
@@ -495,8 +491,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ++st.cnt;
           }
         } else {
-          pf_offer64(sa, sb, j0, be, quarter, lane, cl, kk, two_delta, st);
-          pf_offer64(sc, sd, j0 + 64, be, quarter, lane, cl, kk, two_delta, st);
+          // the maxima of the tile's sixteen 8-score groups (independent), then
+          // one vote: most tiles hold no candidate for any column of the warp
+          float m[16];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            m[g] = max8(sa + 8 * g);
+            m[4 + g] = max8(sb + 8 * g);
+            m[8 + g] = max8(sc + 8 * g);
+            m[12 + g] = max8(sd + 8 * g);
+          }
+          const float mt = fmaxf(max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]),
+                                       max3f(m[6], m[7], m[8])),
+                                 max3f(max3f(m[9], m[10], m[11]), max3f(m[12], m[13], m[14]),
+                                       m[15]));
+          if (__any_sync(kFull, mt > st.thr)) {
+            pf_offer64(sa, sb, m, j0, be, quarter, lane, cl, kk, two_delta, st);
+            pf_offer64(sc, sd, m + 8, j0 + 64, be, quarter, lane, cl, kk, two_delta, st);
+          }
         }
       }
       // survivors of each column (any order) to the workspace
@@ -533,7 +545,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 2 * kPfKeys);
+    tc::tmem_dealloc(tmem, kPfAcc * kPfKeys);
   }
 }
 
