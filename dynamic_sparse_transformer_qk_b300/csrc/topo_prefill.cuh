@@ -15,12 +15,12 @@
 //                            (the scale of the tensor-core rounding bound);
 //   prefill_scan_kernel      persistent; one work item = 128 query columns
 //                            (query row x head pairs of one KV head) against
-//                            all their candidate keys, 128 keys per tile, in
+//                            all their candidate keys, 256 keys per tile, in
 //                            two passes over the same tiles (pass 1 finds
 //                            each column's starting cut from tile maxima):
 //                            M = 128 columns (A: queries, resident in shared
-//                            memory), N = 128 keys (B: K tile by TMA), the
-//                            accumulator in TMEM (four buffers).  Each epilogue
+//                            memory), N = 256 keys (B: K tile by TMA), the
+//                            accumulator in TMEM (two buffers).  Each epilogue
 //                            thread owns one column: it keeps a candidate
 //                            buffer in shared memory, appends every score
 //                            above the column's cut and, when a buffer fills,
@@ -47,13 +47,14 @@
 namespace topo {
 
 constexpr int kPfCols = 128;   // query columns per work item (MMA M)
-constexpr int kPfKeys = 128;   // keys per tile (MMA N)
-constexpr int kPfCap = 96;     // candidate slots per column
+constexpr int kPfKeys = 256;   // keys per tile (MMA N)
+constexpr int kPfSubKeys = 128;  // keys per epilogue step (one TMEM read of a column)
+constexpr int kPfCap = 64;     // candidate slots per column
 constexpr int kPfSub = 8;      // scores offered between room checks
 constexpr int kPfLL = 64;      // survivors published per column
 constexpr int kPfStride = kPfCols + 1;  // buffer row stride (entries)
 constexpr int kPfEpiWarps = 4; // one per TMEM lane quarter
-constexpr int kPfAcc = 4;      // TMEM accumulator buffers (128 columns each)
+constexpr int kPfAcc = 2;      // TMEM accumulator buffers (kPfKeys columns each)
 constexpr int kPfWarps = 2 + kPfEpiWarps;  // + TMA producer + MMA issuer
 constexpr int kPfThreads = 32 * kPfWarps;
 
@@ -391,8 +392,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                  round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
           const long long gs = seq + t;
-          const int ab = (int)(gs & (kPfAcc - 1));
-          const uint32_t around = (uint32_t)(gs >> 2);
+          const int ab = (int)(gs % kPfAcc);
+          const uint32_t around = (uint32_t)(gs / kPfAcc);
           if (!mbar_wait(&acce[ab], (around & 1u) ^ 1u) || !mbar_wait(&full[s], round & 1u)) {
             set_status(G.status, kStatusTimeout);
             misc[0] = 1;
@@ -403,8 +404,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint32_t dt = tmem + (uint32_t)(ab * kPfKeys);
 #pragma unroll
           for (int ks16 = 0; ks16 < KSTEPS; ++ks16) {
-            const uint32_t off = ((ks16 >> 2) * (kPfCols * 128) + (ks16 & 3) * 32) >> 4;
-            tc::mma_bf16(dt, adesc + off, bdesc + off, idesc, ks16 > 0);
+            const uint32_t offa = ((ks16 >> 2) * (kPfCols * 128) + (ks16 & 3) * 32) >> 4;
+            const uint32_t offb = ((ks16 >> 2) * (kPfKeys * 128) + (ks16 & 3) * 32) >> 4;
+            tc::mma_bf16(dt, adesc + offa, bdesc + offb, idesc, ks16 > 0);
           }
           tc::mma_commit(&empty[s]);  // the K stage is free once these MMAs are done
           tc::mma_commit(&accf[ab]);
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       PfState st{0, -INFINITY, 0};
       const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
       // Pass 1 (t < ntiles) offers only the largest score of each tile (one
-      // value per 128 keys); the k-th largest such maximum U is a lower bound
+      // value per 256 keys); the k-th largest such maximum U is a lower bound
       // of the column's k-th best tensor-core score (k distinct keys reach
       // it), so U - 2 delta is a valid starting cut for pass 2, which offers
       // every score of the same tiles.  Both passes compute the same scores
@@ -446,8 +448,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           st.ovf = 0;
         }
         const long long gs = seq + t;
-        const int ab = (int)(gs & (kPfAcc - 1));
-        const uint32_t around = (uint32_t)(gs >> 2);
+        const int ab = (int)(gs % kPfAcc);
+        const uint32_t around = (uint32_t)(gs / kPfAcc);
         const bool ok = __all_sync(kFull, mbar_wait(&accf[ab], around & 1u));
         if (!ok || misc[0]) {
           if (!ok && lane == 0) {
@@ -459,55 +461,64 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc::fence_after_sync();
         const int tt = p1 ? t : t - ntiles;
         const long long j0 = 1 + (long long)tt * kPfKeys;
-        // the whole tile (128 scores of this column) in registers, then the
-        // accumulator goes straight back to the MMA issuer
-        float sa[32], sb[32], sc[32], sd[32];
-        {
-          const uint32_t ta = tq + (uint32_t)(ab * kPfKeys);
-          tc::tmem_ld32(ta, sa);
-          tc::tmem_ld32(ta + 32, sb);
-          tc::tmem_ld32(ta + 64, sc);
-          tc::tmem_ld32(ta + 96, sd);
-          tc::tmem_ld_wait();
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acce[ab]);
-        }
-        if (j0 + kPfKeys - 1 > jhi) {  // keys past the column's last candidate
+        float bm = -INFINITY;
+#pragma unroll 1
+        for (int sub = 0; sub < kPfKeys / kPfSubKeys; ++sub) {
+          // 128 scores of this column in registers; after the last read the
+          // accumulator goes straight back to the MMA issuer
+          float sa[32], sb[32], sc[32], sd[32];
+          const long long js = j0 + sub * kPfSubKeys;
+          {
+            const uint32_t ta = tq + (uint32_t)(ab * kPfKeys + sub * kPfSubKeys);
+            tc::tmem_ld32(ta, sa);
+            tc::tmem_ld32(ta + 32, sb);
+            tc::tmem_ld32(ta + 64, sc);
+            tc::tmem_ld32(ta + 96, sd);
+            tc::tmem_ld_wait();
+            if (sub == kPfKeys / kPfSubKeys - 1) {
+              tc::fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acce[ab]);
+            }
+          }
+          if (js + kPfSubKeys - 1 > jhi) {  // keys past the column's last candidate
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (j0 + i > jhi) sa[i] = -INFINITY;
-            if (j0 + 32 + i > jhi) sb[i] = -INFINITY;
-            if (j0 + 64 + i > jhi) sc[i] = -INFINITY;
-            if (j0 + 96 + i > jhi) sd[i] = -INFINITY;
+            for (int i = 0; i < 32; ++i) {
+              if (js + i > jhi) sa[i] = -INFINITY;
+              if (js + 32 + i > jhi) sb[i] = -INFINITY;
+              if (js + 64 + i > jhi) sc[i] = -INFINITY;
+              if (js + 96 + i > jhi) sd[i] = -INFINITY;
+            }
+          }
+          if (p1) {
+            bm = fmaxf(bm, fmaxf(max64(sa, sb), max64(sc, sd)));
+          } else {
+            // the maxima of the sixteen 8-score groups (independent), then one
+            // vote: most steps hold no candidate for any column of the warp
+            float m[16];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              m[g] = max8(sa + 8 * g);
+              m[4 + g] = max8(sb + 8 * g);
+              m[8 + g] = max8(sc + 8 * g);
+              m[12 + g] = max8(sd + 8 * g);
+            }
+            const float mt = fmaxf(max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]),
+                                         max3f(m[6], m[7], m[8])),
+                                   max3f(max3f(m[9], m[10], m[11]), max3f(m[12], m[13], m[14]),
+                                         m[15]));
+            if (__any_sync(kFull, mt > st.thr)) {
+              pf_offer64(sa, sb, m, js, be, quarter, lane, cl, kk, two_delta, st);
+              pf_offer64(sc, sd, m + 8, js + 64, be, quarter, lane, cl, kk, two_delta, st);
+            }
           }
         }
         if (p1) {
-          const float bm = fmaxf(max64(sa, sb), max64(sc, sd));
           if (__any_sync(kFull, !st.ovf && st.cnt >= kPfCap))
             st = pf_compact_lane(be, cl, kk, two_delta, st, 0, 1, true);
           if (!st.ovf && bm > st.thr) {
             be[st.cnt * kPfStride + cl] = make_float2(bm, __int_as_float(tt));
             ++st.cnt;
-          }
-        } else {
-          // the maxima of the tile's sixteen 8-score groups (independent), then
-          // one vote: most tiles hold no candidate for any column of the warp
-          float m[16];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            m[g] = max8(sa + 8 * g);
-            m[4 + g] = max8(sb + 8 * g);
-            m[8 + g] = max8(sc + 8 * g);
-            m[12 + g] = max8(sd + 8 * g);
-          }
-          const float mt = fmaxf(max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]),
-                                       max3f(m[6], m[7], m[8])),
-                                 max3f(max3f(m[9], m[10], m[11]), max3f(m[12], m[13], m[14]),
-                                       m[15]));
-          if (__any_sync(kFull, mt > st.thr)) {
-            pf_offer64(sa, sb, m, j0, be, quarter, lane, cl, kk, two_delta, st);
-            pf_offer64(sc, sd, m + 8, j0 + 64, be, quarter, lane, cl, kk, two_delta, st);
           }
         }
       }
