@@ -470,10 +470,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const long long js = j0 + sub * kPfSubKeys;
           {
             const uint32_t ta = tq + (uint32_t)(ab * kPfKeys + sub * kPfSubKeys);
-            tc::tmem_ld32(ta, sa);
-            tc::tmem_ld32(ta + 32, sb);
-            tc::tmem_ld32(ta + 64, sc);
-            tc::tmem_ld32(ta + 96, sd);
+            tc::tmem_ld16(ta, *reinterpret_cast<float(*)[16]>(sa));
+            tc::tmem_ld16(ta + 16, *reinterpret_cast<float(*)[16]>(sa + 16));
+            tc::tmem_ld16(ta + 32, *reinterpret_cast<float(*)[16]>(sb));
+            tc::tmem_ld16(ta + 48, *reinterpret_cast<float(*)[16]>(sb + 16));
+            tc::tmem_ld16(ta + 64, *reinterpret_cast<float(*)[16]>(sc));
+            tc::tmem_ld16(ta + 80, *reinterpret_cast<float(*)[16]>(sc + 16));
+            tc::tmem_ld16(ta + 96, *reinterpret_cast<float(*)[16]>(sd));
+            tc::tmem_ld16(ta + 112, *reinterpret_cast<float(*)[16]>(sd + 16));
             tc::tmem_ld_wait();
             if (sub == kPfKeys / kPfSubKeys - 1) {
               tc::fence_before_sync();
