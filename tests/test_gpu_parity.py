@@ -184,12 +184,35 @@ def test_tensor_core_prefill_shapes(name, kw):
     _full(W0.with_(dtype="bf16", **kw))
 
 
-def test_tensor_core_prefill_all_equal_keys_fall_back_exactly():
+@pytest.mark.parametrize("n,nq", [(1200, 200), (20000, 64)])
+def test_tensor_core_prefill_all_equal_keys_fall_back_exactly(n, nq):
     """Every candidate ties: the column buffers overflow and the finalize step
-    rescans those rows exactly; the lowest positions win."""
-    w = W0.with_(dtype="bf16", d=128, Hq=4, Hkv=1, n=1200, nq=200, W=10, k=32)
+    rescans those rows exactly; the lowest positions win.  With n = 20000 the
+    first pass sees more equal tile maxima than its buffer holds (overflow
+    with the cut kept)."""
+    w = W0.with_(dtype="bf16", d=128, Hq=4, Hkv=1, n=n, nq=nq, W=10, k=32)
     x = synth.make(w)
     x["k"][:] = x["k"][:, :, 7:8, :]
+    g = run_gpu(w, x)
+    o = run_oracle(w, x)
+    compare(w, x, g, o)
+
+
+def test_tensor_core_prefill_near_ties():
+    """Prefill rows whose top-k includes keys one mantissa bit apart along a
+    query direction: the tile maxima and the cut they give must keep every
+    key the exact chain ranks in."""
+    w = W0.with_(dtype="bf16", d=128, Hq=8, Hkv=2, n=6000, nq=512, W=64, k=32)
+    x = synth.make(w)
+    rng = np.random.default_rng(7)
+    q0 = synth.widen(x["q"][0, 0, 0], "bf16").astype(np.float64)
+    base = synth.to_bf16_bits(2.0 * np.sqrt(w.d) * q0 / np.linalg.norm(q0))
+    rows = rng.choice(np.arange(1, w.n - w.nq - w.W), size=48, replace=False)
+    for r in rows:
+        kr = base.copy()
+        c = int(rng.integers(0, w.d))
+        kr[c] = np.uint16(int(kr[c]) ^ 1)
+        x["k"][0, 0, r] = kr
     g = run_gpu(w, x)
     o = run_oracle(w, x)
     compare(w, x, g, o)
@@ -295,10 +318,11 @@ def test_chunked_prefill_equals_full_prefill():
         assert torch.allclose(out, full_out[:, :, c * chunk:(c + 1) * chunk], rtol=0, atol=1e-6)
 
 
-def test_chunked_prefill_sampled_rows():
-    """The chunked prefill workload shape (n=65536, 32/8 heads, chunks of 4096),
-    W=64: sampled rows of every chunk against the oracle."""
-    w = synth.CONFIGS[3].with_(W=64)
+@pytest.mark.parametrize("W", [256, 128, 64])
+def test_chunked_prefill_sampled_rows(W):
+    """The chunked prefill workload (n=65536, 32/8 heads, chunks of 4096) at
+    each of its windows: sampled rows of every chunk against the oracle."""
+    w = synth.CONFIGS[3].with_(W=W)
     x = synth.make(w)
     q, k, v = device_inputs(x, w)
     rng = np.random.default_rng(20260211)
