@@ -493,63 +493,6 @@ __device__ __forceinline__ float score_row_smem(const uint8_t* krow, const float
   return acc;
 }
 
-// warp_softmax_pv with every K and V row already staged in shared memory:
-// entry e lives in slot slot_of(e) (negative: skip); slot s holds the K row
-// at stage + s * 2 * ROWB and the V row right after it.
-template <bool BF16, int D, int NC, class Slot>
-__device__ void warp_softmax_pv_staged(const Geom& G, const float2* qd, int hc, long long m,
-                                       Slot&& slot_of, const uint8_t* stage, float* wsm,
-                                       int* jsm, float* outp, int lane) {
-  using S = Shape<BF16, D>;
-  float mrun = -INFINITY, Z = 0.f;
-  float acc[S::EPL];
-#pragma unroll
-  for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
-  for (long long e0 = 0; e0 < m; e0 += 256) {
-    const int cnt = (int)(m - e0 < 256 ? m - e0 : 256);
-    float lmax = -INFINITY;
-    for (int i = lane; i < cnt; i += 32) {
-      const int sl = slot_of(e0 + i);
-      float l = -INFINITY;
-      if (sl >= 0)
-        l = G.scale * score_row_smem<BF16, D, NC>(stage + (size_t)sl * 2 * S::ROWB, qd, hc);
-      wsm[i] = l;
-      jsm[i] = sl;
-      lmax = fmaxf(lmax, l);
-    }
-    lmax = warp_max(lmax);
-    const float mnew = fmaxf(mrun, lmax);
-    __syncwarp();
-    if (mnew == -INFINITY) continue;
-    const float alpha = (mrun == -INFINITY) ? 0.f : expf(mrun - mnew);
-    float zs = 0.f;
-    for (int i = lane; i < cnt; i += 32) {
-      const float l = wsm[i];
-      const float w = (l == -INFINITY) ? 0.f : expf(l - mnew);
-      wsm[i] = w;
-      zs += w;
-    }
-    Z = Z * alpha + warp_sum(zs);
-#pragma unroll
-    for (int e = 0; e < S::EPL; ++e) acc[e] *= alpha;
-    mrun = mnew;
-    __syncwarp();
-#pragma unroll 4
-    for (int i = 0; i < cnt; ++i) {
-      const int sl = jsm[i];
-      if (sl < 0) continue;
-      const float w = wsm[i];
-      float v[S::EPL];
-      lane_elems<BF16, D>(stage + (size_t)sl * 2 * S::ROWB + S::ROWB + lane * S::BPL, v);
-#pragma unroll
-      for (int e = 0; e < S::EPL; ++e) acc[e] = fmaf(w, v[e], acc[e]);
-    }
-    __syncwarp();
-  }
-#pragma unroll
-  for (int e = 0; e < S::EPL; ++e) outp[lane * S::EPL + e] = Z > 0.f ? acc[e] / Z : 0.f;
-}
-
 template <bool BF16, int D, int NC, class Entry>
 __device__ __forceinline__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* qd,
                                                 int hc, long long m, Entry&& entry, float* wsm,
@@ -580,6 +523,10 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
                                          uint8_t* scratch, int scratch_bytes) {
   using S = Shape<BF16, D>;
   constexpr int KP = 32 * KE;
+  // a staged slot: the K row, then the V row, then 16 bytes of padding, so
+  // that consecutive slots start four banks apart (threads scoring
+  // consecutive entries read without bank conflicts)
+  constexpr int SLOT = 2 * S::ROWB + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kk = G.topk;
   const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
@@ -611,7 +558,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   const long long top0 = nb + 1;
   const long long nslots = top0 + (long long)NC * kk;
   const bool fast = (G.flags & kDoPV) && phi >= 0 &&
-                    (long long)off_stage + nslots * 2 * S::ROWB + (long long)NC * mmax * 4 <=
+                    (long long)off_stage + nslots * SLOT + (long long)NC * mmax * 4 <=
                         scratch_bytes;
   uint8_t* stage = scratch + off_stage;
   float* lw = reinterpret_cast<float*>(scratch + off_lw);
@@ -637,7 +584,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
     for (long long sl = tid; sl < top0; sl += blockDim.x) {
       long long row = sl < nb ? band_lo + sl : (band_lo == 0 ? -1 : 0);
       if (row < 0) continue;
-      uint8_t* dst = stage + (size_t)sl * 2 * S::ROWB;
+      uint8_t* dst = stage + (size_t)sl * SLOT;
       bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[1]);
       bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[1]);
     }
@@ -765,7 +712,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       const int h = (int)(sl / kk), i = (int)(sl % kk);
       if (!cols[h].active || i >= tcount[h]) continue;
       const long long row = topj_all[h * KP + i];
-      uint8_t* dst = stage + (size_t)(top0 + sl) * 2 * S::ROWB;
+      uint8_t* dst = stage + (size_t)(top0 + sl) * SLOT;
       bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[2]);
       bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[2]);
     }
@@ -776,7 +723,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
 
   // per-column constants, once: entries m, top-k count t, window start
   int* cm = reinterpret_cast<int*>(scratch + off_lw + NC * mmax * 4);   // [NC] entries
-  int* slot_tab = reinterpret_cast<int*>(stage + nslots * 2 * S::ROWB);  // [NC][mmax]
+  int* slot_tab = reinterpret_cast<int*>(stage + nslots * SLOT);  // [NC][mmax]
   if (tid < NC) {
     const int h = tid;
     const long long p = cols[h].pos;
@@ -799,7 +746,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
     else if (e <= t) sl = top0 + (long long)h * kk + (e - 1);
     else sl = (p - W + 1) + (e - 1 - t) - band_lo;
     slot_tab[i] = (int)sl;
-    lw[i] = scale * score_row_smem<BF16, D, NC>(stage + (size_t)sl * 2 * S::ROWB, qd, h);
+    lw[i] = scale * score_row_smem<BF16, D, NC>(stage + (size_t)sl * SLOT, qd, h);
   }
   __syncthreads();
   // per column: max, weights, normaliser
@@ -830,7 +777,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
     for (int e = 0; e < m; ++e) {
-      const uint8_t* vr = stage + (size_t)st[e] * 2 * S::ROWB + S::ROWB;
+      const uint8_t* vr = stage + (size_t)st[e] * SLOT + S::ROWB;
       float v0, v1;
       if constexpr (BF16) {
         const uint32_t u = *reinterpret_cast<const uint32_t*>(vr + c * 2);
