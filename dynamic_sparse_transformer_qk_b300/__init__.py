@@ -133,8 +133,8 @@ def _check(*ts: torch.Tensor):
             raise ValueError("q, k, v must share one dtype")
 
 
-def _stream(stream) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream, device=None) -> int:
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return s.cuda_stream
 
 
@@ -176,7 +176,7 @@ _default_ws: dict = {}
 
 def _workspace(ws: Workspace | None, device, nbytes: int, stream) -> Workspace:
     if ws is None:
-        key = (device, _stream(stream))
+        key = (device, _stream(stream, device))
         ws = _default_ws.get(key)
         if ws is None:
             ws = _default_ws[key] = Workspace(device, nbytes)
@@ -206,10 +206,11 @@ def forward(q, k, v, *, W: int, topk: int, n: int | None = None, scale: float | 
     if need == 0:
         _raise(-1 if p.d in (64, 128) else -2, "topo_attn_workspace_size")
     ws = _workspace(workspace, q.device, need, stream)
-    rc = lib.topo_attn_forward(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                               out.data_ptr(), idx.data_ptr() if idx is not None else None,
-                               excl.data_ptr() if excl is not None else None, ws.ptr, ws.nbytes,
-                               _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib.topo_attn_forward(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                   out.data_ptr(), idx.data_ptr() if idx is not None else None,
+                                   excl.data_ptr() if excl is not None else None, ws.ptr,
+                                   ws.nbytes, _stream(stream, q.device))
     _raise(rc, "topo_attn_forward")
     return out, idx, excl
 
@@ -227,8 +228,10 @@ def score_select(q, k, *, W: int, topk: int, n: int | None = None, scale: float 
     if need == 0:
         _raise(-1 if p.d in (64, 128) else -2, "topo_attn_workspace_size")
     ws = _workspace(workspace, q.device, need, stream)
-    rc = lib.topo_attn_score_select(ctypes.byref(p), q.data_ptr(), k.data_ptr(), idx.data_ptr(),
-                                    ws.ptr, ws.nbytes, _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib.topo_attn_score_select(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
+                                        idx.data_ptr(), ws.ptr, ws.nbytes,
+                                        _stream(stream, q.device))
     _raise(rc, "topo_attn_score_select")
     return idx
 
@@ -245,9 +248,10 @@ def sparse_softmax_pv(q, k, v, idx, *, W: int, topk: int, n: int | None = None,
         raise ValueError("idx must be contiguous int32 [B, Hq, nq, 1+W+k] on q's device")
     if out is None:
         out = torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q.device)
-    rc = lib.topo_attn_sparse_softmax_pv(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
-                                         v.data_ptr(), idx.data_ptr(), out.data_ptr(),
-                                         _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib.topo_attn_sparse_softmax_pv(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
+                                             v.data_ptr(), idx.data_ptr(), out.data_ptr(),
+                                             _stream(stream, q.device))
     _raise(rc, "topo_attn_sparse_softmax_pv")
     return out
 
@@ -265,8 +269,9 @@ def dense_forward(q, k, v, *, n: int | None = None, scale: float | None = None, 
     if need == 0:
         _raise(-1 if p.d in (64, 128) else -2, "dense_attn_workspace_size")
     ws = _workspace(workspace, q.device, need, stream)
-    rc = lib.dense_attn_forward(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                out.data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib.dense_attn_forward(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                    out.data_ptr(), ws.ptr, ws.nbytes, _stream(stream, q.device))
     _raise(rc, "dense_attn_forward")
     return out
 
@@ -283,11 +288,13 @@ def forward_noalloc(q, k, v, *, W: int, topk: int, n: int | None = None,
     B, Hq, nq, d = q.shape
     if out is None:
         out = torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q.device)
-    rc = lib.topo_attn_forward_noalloc(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
-                                       v.data_ptr(), out.data_ptr(),
-                                       idx.data_ptr() if idx is not None else None,
-                                       excl.data_ptr() if excl is not None else None,
-                                       _stream(stream))
+    # the library looks up its scratch array on the current device: make it q's
+    with torch.cuda.device(q.device):
+        rc = lib.topo_attn_forward_noalloc(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
+                                           v.data_ptr(), out.data_ptr(),
+                                           idx.data_ptr() if idx is not None else None,
+                                           excl.data_ptr() if excl is not None else None,
+                                           _stream(stream, q.device))
     _raise(rc, "topo_attn_forward_noalloc")
     return out, idx, excl
 
@@ -295,6 +302,8 @@ def forward_noalloc(q, k, v, *, W: int, topk: int, n: int | None = None,
 def device_status(ws: Workspace, stream=None) -> int:
     """Read and clear the workspace's device status word (synchronises)."""
     st = ctypes.c_int(0)
-    rc = load_library().topo_attn_device_status(ws.ptr, ctypes.byref(st), _stream(stream))
+    with torch.cuda.device(ws.device):
+        rc = load_library().topo_attn_device_status(ws.ptr, ctypes.byref(st),
+                                                    _stream(stream, ws.device))
     _raise(rc, "topo_attn_device_status")
     return st.value

@@ -30,10 +30,10 @@ struct Plan {
   long long ncols = 0, ncb = 0, units = 0;
   // select (or dense) pass
   long long L = kTile, L2 = kTile, hi_units = 0;
-  int nsplit = 1, stages = 2, smem = 0;
+  int nsplit = 1, stages = 2, ncw = 2, smem = 0;
   // excluded-mass pass
   long long Le = kTile;
-  int nsplit_e = 1, stages_e = 2, smem_e = 0;
+  int nsplit_e = 1, stages_e = 2, ncw_e = 2, smem_e = 0;
   // workspace layout (bytes)
   size_t off_cnt = 0, off_cnt_e = 0, off_kmax = 0, off_work = 0, off_zero_end = 0;
   size_t off_lists = 0, off_thr = 0, off_part = 0, off_surv = 0, off_scnt = 0, off_topk = 0;
@@ -122,6 +122,24 @@ int stages_for(int stage_bytes, int fixed_bytes, int min_ring) {
   return st;
 }
 
+// Ring depth and consumer-warp count of the CUDA-core kernels.  Consumer warp
+// w takes tiles w, w + ncw, ... and tile t uses stage t % stages, so ncw must
+// divide the depth: then a stage is only ever read by one warp, and its
+// previous fill was that warp's own, already consumed (the parity-only
+// barrier wait is unambiguous).  All four warps are used whenever the ring
+// can be rounded down to a multiple of four and still hold `min_ring` bytes.
+void ring_shape(int stage_bytes, int fixed_bytes, int min_ring, int* stages, int* ncw) {
+  int st = stages_for(stage_bytes, fixed_bytes, min_ring);
+  const int w4 = topo::kConsumerWarps;
+  if (st >= w4 && (st - st % w4) * stage_bytes >= min_ring) {
+    *stages = st - st % w4;
+    *ncw = w4;
+    return;
+  }
+  *stages = st;
+  *ncw = st % 3 == 0 ? 3 : (st % 2 == 0 ? 2 : 1);
+}
+
 // Plan for the condensate-set passes (dense=false) or the dense pass.
 int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
   int rc = check_params(p);
@@ -158,7 +176,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
     const int tail = P->NC * P->KP * 8 > P->NC * P->KP * 4 + topo::kWarps * 2048
                          ? P->NC * P->KP * 8
                          : P->NC * P->KP * 4 + topo::kWarps * 2048;
-    P->stages = stages_for(tileb + 16, base.total, tail > 32768 ? tail : 32768);
+    ring_shape(tileb + 16, base.total, tail > 32768 ? tail : 32768, &P->stages, &P->ncw);
     P->smem = topo::Smem(tileb, P->stages, P->D, P->NC, topo::kConsumerWarps * P->NC * cap * 8).total;
     if (P->tc && P->units * 2 <= slots && ncand > (long long)slots * topo::kTcTile) {
       // one wave: every unit gets slots/units splits, the first slots%units one more
@@ -197,7 +215,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
     P->Le = choose_split(P->units, pos_max + 1, slots);
     P->nsplit_e = (int)ceil_div(pos_max + 1, P->Le);
     const topo::Smem base_e(0, 0, P->D, P->NC, topo::kWarps * P->NC * 16);
-    P->stages_e = stages_for(tileb + 16, base_e.total, 32768);
+    ring_shape(tileb + 16, base_e.total, 32768, &P->stages_e, &P->ncw_e);
     P->smem_e = topo::Smem(tileb, P->stages_e, P->D, P->NC, topo::kWarps * P->NC * 16).total;
   } else {
     P->L = choose_split(P->units, pos_max + 1, slots);
@@ -205,7 +223,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
     const int pbuf = topo::kConsumerWarps * kTile * P->NC * 4;
     const topo::Smem base(0, 0, P->D, P->NC, pbuf);
     const int red = topo::kConsumerWarps * P->NC * (P->D + 2) * 4;
-    P->stages = stages_for(2 * tileb + 16, base.total, red > 32768 ? red : 32768);
+    ring_shape(2 * tileb + 16, base.total, red > 32768 ? red : 32768, &P->stages, &P->ncw);
     P->smem = topo::Smem(2 * tileb, P->stages, P->D, P->NC, pbuf).total;
   }
   if (P->smem > topo::kMaxSmem || P->smem_e > topo::kMaxSmem) return TOPO_ERR_UNSUPPORTED;
@@ -348,6 +366,7 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
   G.hi_units = P.hi_units;
   G.nsplit_max = P.nsplit;
   G.stages = P.stages;
+  G.ncw = P.ncw;
   G.flags = (out ? topo::kDoPV : 0) | (idx ? topo::kDoIdx : 0) | (excl ? topo::kSaveThr : 0);
   // split counters, K scales and the work counter start at zero on every call
   rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_zero_end - P.off_cnt, st));
@@ -388,6 +407,7 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
   E.L = P.Le;
   E.nsplit_max = P.nsplit_e;
   E.stages = P.stages_e;
+  E.ncw = P.ncw_e;
   const dim3 grid_e((unsigned)(P.ncb * P.nsplit_e), (unsigned)p->Hkv, (unsigned)p->B);
   return dispatch(P.bf16, P.D, [&](auto L) { return L.excl(P.NC, mk, E, grid_e, P.smem_e, st); });
 }
@@ -472,6 +492,7 @@ int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, 
   G.L = P.L;
   G.nsplit_max = P.nsplit;
   G.stages = P.stages;
+  G.ncw = P.ncw;
   const dim3 grid((unsigned)(P.ncb * P.nsplit), (unsigned)p->Hkv, (unsigned)p->B);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_part - P.off_cnt, st));

@@ -42,6 +42,7 @@ struct Geom {
   long long hi_units;     // units that use L2 (one more split each); 0: none
   int nsplit_max;         // grid.x = ncb * nsplit_max
   int stages;             // ring depth
+  int ncw;                // consumer warps that score tiles (1..kConsumerWarps; divides stages)
   int flags;
   const void* qp;
   const void* kp;
@@ -303,14 +304,19 @@ __device__ __forceinline__ void drain_tiles(int issued, int stages, uint64_t* fu
   }
 }
 
-// Consumer loop of warp `warp`: tiles warp, warp+4, ...; body(t, stage_ptr).
+// Consumer loop of warp `warp` (< ncw): tiles warp, warp+ncw, ...;
+// body(t, stage_ptr).  ncw divides `stages`, so every stage is only ever read
+// by one warp and tile t - stages (the previous fill of t's stage) is this
+// warp's own, already consumed: the parity wait below cannot match a phase two
+// fills old.  Warps >= ncw take no tiles.
 template <class Body>
-__device__ __forceinline__ void consume_tiles(int warp, int ntiles, int stages, int stage_bytes,
-                                              uint8_t* ring, uint64_t* full, uint64_t* empty,
-                                              volatile int* abort_flag, int* status,
-                                              Body&& body) {
+__device__ __forceinline__ void consume_tiles(int warp, int ncw, int ntiles, int stages,
+                                              int stage_bytes, uint8_t* ring, uint64_t* full,
+                                              uint64_t* empty, volatile int* abort_flag,
+                                              int* status, Body&& body) {
   const int lane = threadIdx.x & 31;
-  for (int t = warp; t < ntiles; t += kConsumerWarps) {
+  if (warp >= ncw) return;
+  for (int t = warp; t < ntiles; t += ncw) {
     const int s = t % stages;
     const uint32_t round = (uint32_t)(t / stages);
     const bool ok = __all_sync(kFull, mbar_wait(&full[s], round & 1u));
@@ -865,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long jh[NC];
 #pragma unroll
     for (int h = 0; h < NC; ++h) jh[h] = cols[h].jhi < ke ? cols[h].jhi : ke;
-    consume_tiles(warp, ntiles, G.stages, S::TILEB, ring, full, empty, misc, G.status,
+    consume_tiles(warp, G.ncw, ntiles, G.stages, S::TILEB, ring, full, empty, misc, G.status,
                   [&](int t, const uint8_t* tile) {
                     float2 acc[NC];
                     score_tile<BF16, D, NC>(tile, qd, lane, acc);
@@ -1012,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       lim[h] = p < ke ? p : ke;
       wlo[h] = p - G.W + 1;
     }
-    consume_tiles(warp, ntiles, G.stages, S::TILEB, ring, full, empty, misc, G.status,
+    consume_tiles(warp, G.ncw, ntiles, G.stages, S::TILEB, ring, full, empty, misc, G.status,
                   [&](int t, const uint8_t* tile) {
                     float2 acc[NC];
                     score_tile<BF16, D, NC>(tile, qd, lane, acc);
@@ -1131,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long p = cols[h].active ? cols[h].pos : -1;
       lim[h] = p < ke ? p : ke;
     }
-    consume_tiles(warp, ntiles, G.stages, 2 * S::TILEB, ring, full, empty, misc, G.status,
+    consume_tiles(warp, G.ncw, ntiles, G.stages, 2 * S::TILEB, ring, full, empty, misc, G.status,
                   [&](int t, const uint8_t* stage) {
                     float2 sc[NC];
                     score_tile<BF16, D, NC>(stage, qd, lane, sc);

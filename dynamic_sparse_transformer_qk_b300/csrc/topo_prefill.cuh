@@ -16,8 +16,8 @@
 //   prefill_scan_kernel      persistent; one work item = 128 query columns
 //                            (query row x head pairs of one KV head) against
 //                            all their candidate keys, 256 keys per tile, in
-//                            two passes over the same tiles (pass 1 finds
-//                            each column's starting cut from tile maxima):
+//                            two passes (pass 1 finds each column's starting
+//                            cut from the maxima of every second tile):
 //                            M = 128 columns (A: queries, resident in shared
 //                            memory), N = 256 keys (B: K tile by TMA), the
 //                            accumulator in TMEM (two buffers).  Each epilogue
@@ -54,6 +54,7 @@ constexpr int kPfSub = 8;      // scores offered between room checks
 constexpr int kPfLL = 64;      // survivors published per column
 constexpr int kPfStride = kPfCols + 1;  // buffer row stride (entries)
 constexpr int kPfEpiWarps = 4; // one per TMEM lane quarter
+constexpr int kPfP1Stride = 2; // the first pass reads every kPfP1Stride-th tile
 constexpr int kPfAcc = 2;      // TMEM accumulator buffers (kPfKeys columns each)
 constexpr int kPfWarps = 2 + kPfEpiWarps;  // + TMA producer + MMA issuer
 constexpr int kPfThreads = 32 * kPfWarps;
@@ -319,22 +320,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tmem = *tslot;
 
   long long seq = 0;  // tiles this CTA has run (phases of the ring and accumulator barriers)
-  const int nbh = G.B * G.Hkv;
   for (;;) {
     __syncthreads();
     if (tid == 0) misc[2] = atomicAdd(G.work, 1);
     __syncthreads();
     const long long item = misc[2];
     if (item >= G.nitems || misc[0]) break;
-    // the longest blocks (latest rows) first
-    const int bh = (int)(item % nbh);
-    const int blk = G.items_per_head - 1 - (int)(item / nbh);
+    // one KV head at a time (its K tiles stay in L2 for the CTAs that share
+    // it), the longest blocks (latest rows) of each head first
+    const int bh = (int)(item / G.items_per_head);
+    const int blk = G.items_per_head - 1 - (int)(item % G.items_per_head);
     const int b = bh / G.Hkv, kvh = bh % G.Hkv;
     const long long c0 = (long long)blk * kPfCols;
     const long long cend = (c0 + kPfCols < G.ncols) ? c0 + kPfCols : G.ncols;
     const long long r_last = (cend - 1) / G.g;
     const long long jmax = G.n - G.nq + r_last - G.W;
     const int ntiles = jmax >= 1 ? (int)((jmax + kPfKeys - 1) / kPfKeys) : 0;
+    // pass 1 reads tiles 0, S, 2S, ... (S = kPfP1Stride); pass 2 every tile
+    const int n1 = (ntiles + kPfP1Stride - 1) / kPfP1Stride;
     const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
 
     // queries of the block: bf16, K-major, 128-byte swizzle; missing columns zero
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // ring slot and round of tile seq + t, advanced without a division per tile
         int s = (int)(seq % stages);
         uint32_t round = (uint32_t)(seq / stages);
-        for (int t = 0; t < 2 * ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
+        for (int t = 0; t < n1 + ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
                  round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
           if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           uint8_t* dst = ring + (size_t)s * TILEB;
           mbar_arrive_expect_tx(&full[s], (uint32_t)TILEB);
-          const int tt = t < ntiles ? t : t - ntiles;  // both passes run the same tiles
+          const int tt = t < n1 ? t * kPfP1Stride : t - n1;
           const int y = (int)(kvrow0 + 1 + (long long)tt * kPfKeys);
 #pragma unroll
           for (int cc = 0; cc < S::NCH; ++cc)
@@ -388,7 +391,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const uint64_t bdesc0 = tc::smem_desc_sw128(smem_addr(ring));
         int s = (int)(seq % stages);
         uint32_t round = (uint32_t)(seq / stages);
-        for (int t = 0; t < 2 * ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
+        for (int t = 0; t < n1 + ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
                  round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
           const long long gs = seq + t;
@@ -434,15 +437,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float two_delta = 2.f * tc_delta_factor(D) * qn1 * 1.001f * kmx;
       PfState st{0, -INFINITY, 0};
       const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
-      // Pass 1 (t < ntiles) offers only the largest score of each tile (one
-      // value per 256 keys); the k-th largest such maximum U is a lower bound
-      // of the column's k-th best tensor-core score (k distinct keys reach
-      // it), so U - 2 delta is a valid starting cut for pass 2, which offers
-      // every score of the same tiles.  Both passes compute the same scores
+      // Pass 1 (t < n1) offers only the largest score of each of its tiles
+      // (every kPfP1Stride-th tile, one value per 256 keys); the k-th largest
+      // such maximum U is a lower bound of the column's k-th best tensor-core
+      // score (k distinct keys reach it, whichever tiles they came from), so
+      // U - 2 delta is a valid starting cut for pass 2, which offers every
+      // score of every tile.  Both passes compute the same scores for a tile
       // (identical operands and instruction sequence).
-      for (int t = 0; t < 2 * ntiles; ++t) {
-        const bool p1 = t < ntiles;
-        if (t == ntiles) {
+      for (int t = 0; t < n1 + ntiles; ++t) {
+        const bool p1 = t < n1;
+        if (t == n1) {
           st = pf_compact_lane(be, cl, kk, two_delta, st, 0, 0, true);
           st.cnt = 0;
           st.ovf = 0;
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const int tt = p1 ? t : t - ntiles;
+        const int tt = p1 ? t * kPfP1Stride : t - n1;
         const long long j0 = 1 + (long long)tt * kPfKeys;
         float bm = -INFINITY;
 #pragma unroll 1
@@ -546,7 +550,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) G.surv_cnt[gcol] = ovl ? -1 : cnt_c;
       }
     }
-    seq += 2 * ntiles;
+    seq += n1 + ntiles;
   }
 
   // no copy into shared memory and no MMA may outlive the CTA

@@ -162,7 +162,10 @@ int dense_attn_forward(const topo_attn_params *p, const void *q, const void *k, 
  *
  * Set-up: the first call on a device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress and caches it.  Make that
- * first call before any stream capture on that device.
+ * first call before any stream capture on that device.  The current device
+ * must be the one that owns q, k, v and out.  The cached address belongs to
+ * the device's primary context: after cudaDeviceReset (which destroys that
+ * context) it is stale, so do not use this entry point again in that process.
  *
  * Sharing: every call, on every stream and host thread, uses the same array,
  * which keeps the previous call's contents; each call clears what must start

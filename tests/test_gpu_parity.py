@@ -86,6 +86,8 @@ EDGE = [
     ("gqa_16_decode", dict(n=2000, nq=1, Hq=16, Hkv=1, W=5, k=9)),
     ("batch_3", dict(B=3, n=333, nq=333, Hq=2, Hkv=1, W=4, k=6)),
     ("d128_f32", dict(d=128, n=600, nq=600, W=12, k=10)),
+    ("d128_f32_k200_nq8", dict(d=128, n=3000, nq=8, W=16, k=200)),
+    ("d128_f32_k256_gqa", dict(d=128, n=2500, nq=2, Hq=8, Hkv=2, W=5, k=256)),
     ("kv_stride_nan_tail", dict(n=555, nq=555, kv_stride=700, nan_tail=True, W=6, k=9)),
     ("bf16_d64", dict(dtype="bf16", n=800, nq=800, W=11, k=13)),
     ("bf16_d128_gqa4", dict(dtype="bf16", d=128, Hq=8, Hkv=2, n=900, nq=900, W=16, k=16)),
@@ -290,7 +292,9 @@ def test_sparse_softmax_pv_ignores_out_of_range_entries():
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(dtype="bf16", d=128, Hq=8, Hkv=2),
-                                dict(n=3000, nq=1, Hq=4, Hkv=1), dict(n=1, nq=1)])
+                                dict(n=3000, nq=1, Hq=4, Hkv=1), dict(n=1, nq=1),
+                                dict(d=128, n=32768, nq=1), dict(d=128, n=5000, nq=8),
+                                dict(d=128, n=4000, nq=3, Hq=8, Hkv=2)])
 def test_dense_matches_oracle(kw):
     w = W0.with_(n=700, nq=700).with_(**kw)
     x = synth.make(w)
@@ -318,28 +322,87 @@ def test_chunked_prefill_equals_full_prefill():
         assert torch.allclose(out, full_out[:, :, c * chunk:(c + 1) * chunk], rtol=0, atol=1e-6)
 
 
+def _run_chunks(w, x, keep_rows):
+    """The chunked prefill (chunks of w.chunk rows through topo_attn_forward,
+    idx and excluded mass on) on the device; returns idx, out and excl of the
+    flat rows `keep_rows` (ids over [B=1, Hq, n])."""
+    q, k, v = device_inputs(x, w)
+    keep_rows = np.asarray(keep_rows)
+    heads, pos = keep_rows // w.n, keep_rows % w.n
+    res = {"idx": np.empty((keep_rows.size, 1 + w.W + w.k), np.int32),
+           "out": np.empty((keep_rows.size, w.d), np.float32),
+           "excl": np.empty(keep_rows.size, np.float32)}
+    chunk = w.chunk
+    for c in range(w.n // chunk):
+        sel = np.nonzero((pos >= c * chunk) & (pos < (c + 1) * chunk))[0]
+        if sel.size == 0:
+            continue
+        qc = q[:, :, c * chunk:(c + 1) * chunk].contiguous()
+        out, idx, excl = topo.forward(qc, k, v, W=w.W, topk=w.k, n=(c + 1) * chunk,
+                                      scale=w.scale, want_idx=True, want_excl=True)
+        torch.cuda.synchronize()
+        h = torch.from_numpy(heads[sel]).cuda()
+        r = torch.from_numpy(pos[sel] - c * chunk).cuda()
+        res["idx"][sel] = idx[0][h, r].cpu().numpy()
+        res["out"][sel] = out[0][h, r].cpu().numpy()
+        res["excl"][sel] = excl[0][h, r].cpu().numpy()
+    return res
+
+
 @pytest.mark.parametrize("W", [256, 128, 64])
-def test_chunked_prefill_sampled_rows(W):
+def test_chunked_prefill_first_chunk_and_sampled_rows(W):
     """The chunked prefill workload (n=65536, 32/8 heads, chunks of 4096) at
-    each of its windows: sampled rows of every chunk against the oracle."""
+    each of its windows, against the oracle: every row of every head in the
+    first chunk, plus 512 seeded rows spread over all 16 chunks (32 per chunk,
+    any head) -- idx bit for bit, out within 2e-3 row-relative, the excluded
+    mass within 1e-6 + 1e-4 eps."""
     w = synth.CONFIGS[3].with_(W=W)
     x = synth.make(w)
-    q, k, v = device_inputs(x, w)
-    rng = np.random.default_rng(20260211)
-    chunk = w.chunk
-    got_idx = np.empty((w.Hq, w.n, 1 + w.W + w.k), np.int32)
-    got_out = np.empty((w.Hq, w.n, w.d), np.float32)
-    for c in range(w.n // chunk):
-        qc = q[:, :, c * chunk:(c + 1) * chunk].contiguous()
-        out, idx, _ = topo.forward(qc, k, v, W=w.W, topk=w.k, n=(c + 1) * chunk, scale=w.scale,
-                                   want_idx=True)
-        got_idx[:, c * chunk:(c + 1) * chunk] = idx[0].cpu().numpy()
-        got_out[:, c * chunk:(c + 1) * chunk] = out[0].cpu().numpy()
-    rows = np.sort(rng.choice(w.Hq * w.n, size=256, replace=False))
+    rng = np.random.default_rng(20260211 + W)
+    first = (np.arange(w.Hq)[:, None] * w.n + np.arange(w.chunk)[None, :]).reshape(-1)
+    sampled = []
+    for c in range(w.n // w.chunk):
+        hh = rng.integers(0, w.Hq, 32)
+        rr = rng.choice(np.arange(c * w.chunk, (c + 1) * w.chunk), 32, replace=False)
+        sampled.append(hh * w.n + rr)
+    rows = np.unique(np.concatenate([first] + sampled))
+    assert rows.size >= first.size + 480
+    g = _run_chunks(w, x, rows)
     o = oracle.topo_attn(oracle_params(w), x["q"], x["k"], x["v"], rows=rows,
-                         want=("out", "idx"))
-    np.testing.assert_array_equal(got_idx.reshape(-1, 1 + w.W + w.k)[rows], o["idx"])
-    assert_out_close(got_out.reshape(-1, w.d)[rows], o["out"], w.dtype)
+                         want=("out", "idx", "excl"))
+    compare(w, x, g, o)
+
+
+def test_chunked_prefill_full_size_near_ties():
+    """The last 4096-row chunk of the 64K prefill (W=64) with 48 keys one
+    mantissa bit apart along one query's direction: every row of that query's
+    head and a seeded sample of the others must keep exactly the oracle's
+    top-k, although the tensor-core scores cannot separate those keys."""
+    w = synth.CONFIGS[3].with_(W=64)
+    x = synth.make(w)
+    rng = np.random.default_rng(31)
+    p0 = w.n - w.chunk
+    q0 = synth.widen(x["q"][0, 0, p0], "bf16").astype(np.float64)
+    base = synth.to_bf16_bits(2.0 * np.sqrt(w.d) * q0 / np.linalg.norm(q0))
+    for r in rng.choice(np.arange(1, p0 - w.W), size=48, replace=False):
+        kr = base.copy()
+        c = int(rng.integers(0, w.d))
+        kr[c] = np.uint16(int(kr[c]) ^ 1)
+        x["k"][0, 0, r] = kr
+    q, k, v = device_inputs(x, w)
+    qc = q[:, :, p0:].contiguous()
+    out, idx, excl = topo.forward(qc, k, v, W=w.W, topk=w.k, n=w.n, scale=w.scale,
+                                  want_idx=True, want_excl=True)
+    torch.cuda.synchronize()
+    head0 = np.arange(w.chunk)                                   # head 0: every row
+    others = rng.choice(np.arange(w.chunk, w.Hq * w.chunk), 512, replace=False)
+    sel = np.sort(np.concatenate([head0, others]))
+    hh, rr = sel // w.chunk, sel % w.chunk
+    g = {"idx": idx[0].cpu().numpy()[hh, rr], "out": out[0].cpu().numpy()[hh, rr],
+         "excl": excl[0].cpu().numpy()[hh, rr]}
+    o = oracle.topo_attn(oracle_params(w), x["q"], x["k"], x["v"], rows=hh * w.n + p0 + rr,
+                         want=("out", "idx", "excl"))
+    compare(w, x, g, o)
 
 
 # ------------------------------------------------ repeatability and status --
