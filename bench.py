@@ -259,18 +259,30 @@ def traffic_from_profile(kernel: str, workload: str):
     return None
 
 
-def bench_ours(args, w: synth.Workload):
+def decode_alg_bytes(w: synth.Workload) -> int:
+    """Algorithmic bytes of one decode step: K read once, the 1+W+k V rows of
+    C_i per query head, the anchor and window K rows per KV head (logits), q
+    in and out."""
+    es = 2 if w.dtype == "bf16" else 4
+    cset = min(w.n, 1 + w.W + w.k)
+    k_bytes = w.B * w.Hkv * w.n * w.d * es
+    gather = w.B * w.Hq * cset * w.d * es + w.B * w.Hkv * (1 + w.W) * w.d * es
+    io = w.B * w.Hq * w.d * (es + 4)
+    return k_bytes + gather + io
+
+
+def measure_decode(args, w: synth.Workload, dev, rank: int, world: int, local: int, *,
+                   steps: int, e2e: bool = True, dense: bool = True,
+                   cpu_budget: float = 0.0, x: dict | None = None) -> dict:
+    """One decode step per sequence through topo_attn_forward, timed as CUDA
+    graph replays with CUDA events; returns the figures of one JSON record."""
     import torch
     import torch.distributed as dist
     import dynamic_sparse_transformer_qk_b300 as topo
 
-    world, rank, local = dist_env()
-    if world > 1:
-        dist.init_process_group("gloo", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    # every rank serves its own sequences (weak scaling, no data-path collective)
-    x = synth.make(rank_workload(w, rank))
+    if x is None:
+        # every rank serves its own sequences (weak scaling, no data-path collective)
+        x = synth.make(rank_workload(w, rank))
 
     def to_dev(a):
         t = torch.from_numpy(a)
@@ -293,18 +305,19 @@ def bench_ours(args, w: synth.Workload):
     with torch.cuda.graph(graph):
         step()
     torch.cuda.synchronize()
-    es_ = 2 if w.dtype == "bf16" else 4
-    l2_flush = w.B * w.Hkv * w.n * w.d * es_ < 2 * 126 * 2 ** 20
+    es = 2 if w.dtype == "bf16" else 4
+    k_bytes = w.B * w.Hkv * w.n * w.d * es
+    l2_flush = k_bytes < 2 * 126 * 2 ** 20
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev) if l2_flush else None
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         time.sleep(0.3)
         t_wall = time.perf_counter()
-        for i in range(args.steps):
+        for i in range(steps):
             if flush is not None:
                 flush.zero_()  # evict the K cache from L2 between timed steps
             ev[i][0].record(stream)
@@ -314,7 +327,7 @@ def bench_ours(args, w: synth.Workload):
         t_wall = time.perf_counter() - t_wall
         # keep sampling a moment so short regions still get clock samples
         if t_wall < 0.5 and not args.profile:
-            extra = max(1, int(0.5 / max(t_wall / args.steps, 1e-6)))
+            extra = max(1, int(0.5 / max(t_wall / steps, 1e-6)))
             for _ in range(min(extra, 20000)):
                 graph.replay()
             torch.cuda.synchronize()
@@ -322,14 +335,7 @@ def bench_ours(args, w: synth.Workload):
     ms, value = job_rate(sum(per) / len(per), w.B, world)
     queries = w.B * world
 
-    # dominant kernel roofline: the fused select kernel streams K once and
-    # gathers the 1+W+k V rows (and the anchor/window K rows) per query head
-    es = 2 if w.dtype == "bf16" else 4
-    cset = min(w.n, 1 + w.W + w.k)
-    k_bytes = w.B * w.Hkv * w.n * w.d * es
-    gather = w.B * w.Hq * cset * w.d * es + w.B * w.Hkv * (1 + w.W) * w.d * es
-    io = w.B * w.Hq * w.d * (es + 4)
-    alg_bytes = k_bytes + gather + io
+    alg_bytes = decode_alg_bytes(w)
     peaks = load_peaks()
     achieved = alg_bytes / (ms / 1000.0) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -339,50 +345,53 @@ def bench_ours(args, w: synth.Workload):
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "timing": "CUDA events around each replay of the captured step "
                           "(one counter memset + one kernel)",
-                "traffic": traffic_from_profile("topo_select_tc_kernel", "decode-1m")}
-
+                "traffic": traffic_from_profile("topo_select_tc_kernel",
+                                                "decode-1m" if w.n == 1048576 and w.B == 1
+                                                else "none")}
+    rec = {"ms_per_step": ms, "value": value, "unit": "queries/s", "roofline": roofline,
+           "clocks": clk.summary(), "queries_per_step": queries, "gpu_launches": steps,
+           "config": {"workload": workload_desc(w),
+                      "l2": (f"K cache {k_bytes / 1e9:.3f} GB < 2x L2: 256 MB write between "
+                             "timed steps" if l2_flush else
+                             f"K cache {k_bytes / 1e9:.2f} GB per GPU >> 126 MB L2; no flush")}}
     if args.profile:
-        if rank == 0:
-            print(json.dumps({"profile": True, "ms_per_step": ms, "value": value,
-                              "workload": workload_desc(w)}), flush=True)
-        return
-    # end to end through the public API: pinned host q and the appended K/V
-    # row go up, out comes back, every step
-    hq = torch.from_numpy(x["q"]).pin_memory()
-    hk_row = torch.from_numpy(np.ascontiguousarray(x["k"][:, :, w.n - 1])).pin_memory()
-    hv_row = torch.from_numpy(np.ascontiguousarray(x["v"][:, :, w.n - 1])).pin_memory()
-    hout = torch.empty_like(out, device="cpu").pin_memory()
-    kview = k.view(torch.uint16) if w.dtype == "bf16" else k
-    vview = v.view(torch.uint16) if w.dtype == "bf16" else v
-    qview = q.view(torch.uint16) if w.dtype == "bf16" else q
+        return rec
+    if e2e:
+        # end to end through the public API: pinned host q and the appended K/V
+        # row go up, out comes back, every step
+        hq = torch.from_numpy(x["q"]).pin_memory()
+        hk_row = torch.from_numpy(np.ascontiguousarray(x["k"][:, :, w.n - 1])).pin_memory()
+        hv_row = torch.from_numpy(np.ascontiguousarray(x["v"][:, :, w.n - 1])).pin_memory()
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        kview = k.view(torch.uint16) if w.dtype == "bf16" else k
+        vview = v.view(torch.uint16) if w.dtype == "bf16" else v
+        qview = q.view(torch.uint16) if w.dtype == "bf16" else q
 
-    def e2e_step():
-        qview.copy_(hq, non_blocking=True)
-        kview[:, :, w.n - 1].copy_(hk_row, non_blocking=True)
-        vview[:, :, w.n - 1].copy_(hv_row, non_blocking=True)
-        step()
-        hout.copy_(out, non_blocking=True)
+        def e2e_step():
+            qview.copy_(hq, non_blocking=True)
+            kview[:, :, w.n - 1].copy_(hk_row, non_blocking=True)
+            vview[:, :, w.n - 1].copy_(hv_row, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
 
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ems, _ = job_rate(e0.elapsed_time(e1) / args.steps, w.B, world)
-    h2d = hq.numel() * hq.element_size() + 2 * hk_row.numel() * hk_row.element_size()
-    d2h = hout.numel() * hout.element_size()
-    e2e = {"value": queries / (ems / 1000.0), "unit": "queries/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
-
-    # the dense (full attention) path on the same cache, for comparison
-    dense_ms = None
-    if args.dense:
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems, _ = job_rate(e0.elapsed_time(e1) / steps, w.B, world)
+        h2d = hq.numel() * hq.element_size() + 2 * hk_row.numel() * hk_row.element_size()
+        d2h = hout.numel() * hout.element_size()
+        rec["e2e"] = {"value": queries / (ems / 1000.0), "unit": "queries/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if dense:
+        # the dense (full attention) path on the same cache, for comparison
         dout = torch.empty_like(out)
         dws = topo.Workspace(dev)
         for _ in range(3):
@@ -392,7 +401,7 @@ def bench_ours(args, w: synth.Workload):
         with torch.cuda.graph(dgraph):
             topo.dense_forward(q, k, v, n=w.n, scale=w.scale, out=dout, workspace=dws)
         torch.cuda.synchronize()
-        nd = max(3, args.steps // 4)
+        nd = max(3, steps // 4)
         dsum = 0.0
         for _ in range(nd):
             if flush is not None:
@@ -404,52 +413,96 @@ def bench_ours(args, w: synth.Workload):
             torch.cuda.synchronize()
             dsum += d0.elapsed_time(d1)
         dense_ms = dsum / nd
+        dense_bytes = 2 * k_bytes + w.B * w.Hq * w.d * (es + 4)
+        rec["dense_attn"] = {"ms_per_step": dense_ms,
+                             "gbs": dense_bytes / (dense_ms / 1000.0) / 1e9,
+                             "hbm_frac": dense_bytes / (dense_ms / 1000.0) / 1e9
+                             / peaks["hbm_gbs"],
+                             "sparse_speedup": dense_ms / ms}
+    if rank == 0 and world == 1 and cpu_budget > 0:
+        rec["cpu_baseline"] = oracle_rate(w, x, budget_s=cpu_budget)
+    del q, k, v
+    return rec
 
+
+def bench_ours(args, w: synth.Workload):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rec = measure_decode(args, w, dev, rank, world, local, steps=args.steps,
+                         dense=args.dense and not args.profile,
+                         cpu_budget=0.0 if args.no_cpu_baseline else args.cpu_budget)
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile": True, "ms_per_step": rec["ms_per_step"],
+                              "value": rec["value"], "workload": workload_desc(w)}), flush=True)
+        return
+    subs = []
+    if world == 1 and args.workloads:
+        # the other workloads of the benchmark, one sub-record each (same
+        # rules: inputs resident in HBM, CUDA events, clocks sampled)
+        sub_steps = max(3, min(args.steps, 10))
+        bcfg = synth.CONFIGS[2]
+        r = measure_decode(args, bcfg, dev, rank, world, local, steps=args.steps, e2e=True,
+                           dense=True, cpu_budget=0.0 if args.no_cpu_baseline else 5.0)
+        subs.append(dict(name="decode-128k-b16", metric=METRIC, **r))
+        torch.cuda.empty_cache()
+        r = measure_decode(args, synth.CONFIGS[1], dev, rank, world, local, steps=args.steps,
+                           e2e=True, dense=True,
+                           cpu_budget=0.0 if args.no_cpu_baseline else 5.0)
+        subs.append(dict(name="decode-32k", metric=METRIC, **r))
+        torch.cuda.empty_cache()
+        px = synth.make(synth.CONFIGS[3])
+        for W in synth.PREFILL_WINDOWS:
+            wp = synth.CONFIGS[3].with_(W=W)
+            r = measure_prefill(args, wp, dev, local, steps=sub_steps, x=px, e2e=False,
+                                cpu_budget=0.0 if args.no_cpu_baseline else 5.0)
+            subs.append(dict(name=f"prefill-64k-W{W}", metric=PREFILL_METRIC, **r))
+            torch.cuda.empty_cache()
+        del px
     if rank != 0:
         if world > 1:
             dist.barrier()
         return
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_rate(w, x, budget_s=args.cpu_budget)
     line = {
-        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "metric": METRIC, "value": rec["value"], "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
         if w.dtype == "bf16" else "f32",
         "data": "synthetic: seeded N(0,1) Q/K/V, Q+=3u, sink K[0]+=6u, "
                 f"{w.planted} planted keys per KV head",
-        "config": {"workload": workload_desc(w), "queries_per_step": queries,
-                   "l2": (f"K cache {k_bytes / 1e9:.3f} GB < 2x L2: 256 MB write between timed "
-                          "steps" if l2_flush else
-                          f"K cache {k_bytes / 1e9:.2f} GB per GPU >> 126 MB L2; no flush"),
-                   "timed_outputs": "out only (idx and excluded mass off the timed path)"},
-        "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peaks["hbm_gbs"],
-        "roofline": roofline, "e2e": e2e, "clocks": clk.summary(),
-        "gpu_launches": args.steps, "cpu_baseline": cpu,
+        "config": dict(rec["config"], queries_per_step=rec["queries_per_step"],
+                       timed_outputs="out only (idx and excluded mass off the timed path)"),
+        "hbm_gbs": rec["roofline"]["achieved"], "hbm_frac_of_peak": rec["roofline"]["frac"],
+        "roofline": rec["roofline"], "e2e": rec.get("e2e"), "clocks": rec["clocks"],
+        "gpu_launches": rec["gpu_launches"], "cpu_baseline": rec.get("cpu_baseline"),
     }
-    if dense_ms is not None:
-        dense_bytes = 2 * k_bytes + io
-        line["dense_attn"] = {"ms_per_step": dense_ms,
-                              "gbs": dense_bytes / (dense_ms / 1000.0) / 1e9,
-                              "sparse_speedup": dense_ms / ms}
+    if "dense_attn" in rec:
+        line["dense_attn"] = rec["dense_attn"]
+    if subs:
+        line["workloads"] = subs
+    elif world > 1:
+        line["workloads_note"] = "sub-workloads are measured at N=1 only"
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
 
 
-def bench_prefill(args, w: synth.Workload):
+def measure_prefill(args, w: synth.Workload, dev, local: int, *, steps: int,
+                    x: dict | None = None, e2e: bool = True, cpu_budget: float = 0.0) -> dict:
     """Chunked causal prefill (n=65536, chunks of 4096 rows): one step = the
-    whole sequence through topo_attn_forward, chunk by chunk."""
+    whole sequence through topo_attn_score_select (the scored value) and
+    through topo_attn_forward (reported beside it), chunk by chunk."""
     import torch
     import dynamic_sparse_transformer_qk_b300 as topo
 
-    world, rank, local = dist_env()
-    if rank != 0:
-        return
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    x = synth.make(w)
+    if x is None:
+        x = synth.make(w)
 
     def to_dev(a):
         return torch.from_numpy(a).view(torch.bfloat16).to(dev)
@@ -480,29 +533,27 @@ def bench_prefill(args, w: synth.Workload):
     if args.profile:
         # profiling: the last chunk call alone (warm-up calls, then `steps` calls)
         c = nch - 1
-        for _ in range(args.warmup + args.steps):
+        for _ in range(args.warmup + steps):
             topo.forward(qs[c], k, v, W=w.W, topk=w.k, n=(c + 1) * chunk, scale=w.scale,
                          out=obufs[c], workspace=ws)
         torch.cuda.synchronize()
-        print(json.dumps({"profile": True, "workload": workload_desc(w), "chunk_call": c}),
-              flush=True)
-        return
+        return {"profile": True, "workload": workload_desc(w), "chunk_call": c}
 
-    def timed(fn, steps):
+    def timed(fn, nsteps):
         for _ in range(args.warmup):
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(steps):
+        for _ in range(nsteps):
             fn()
         e1.record(stream)
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / steps
+        return e0.elapsed_time(e1) / nsteps
 
     with ClockSampler(local) as clk:
-        ms = timed(step, args.steps)
-        sel_ms = timed(select_step, args.steps)
+        ms = timed(step, steps)
+        sel_ms = timed(select_step, steps)
     flops = 2.0 * w.Hq * w.d * (w.n * (w.n + 1) / 2.0) * w.B
     peaks = load_peaks()
     value = flops / (sel_ms / 1000.0) / 1e12
@@ -511,43 +562,65 @@ def bench_prefill(args, w: synth.Workload):
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst)",
                 "kernel": "prefill_scan_kernel (+ K-scale and exact-rescoring finalize)",
                 "algorithmic_flops_per_step": flops,
-                "timing": "CUDA events around 16 topo_attn_score_select chunk calls",
+                "timing": f"CUDA events around {nch} topo_attn_score_select chunk calls",
                 "traffic": None}
-    # end to end: the sequence's q, k, v go up from pinned host memory, out comes back
-    hq = torch.from_numpy(x["q"]).pin_memory()
-    hk = torch.from_numpy(x["k"]).pin_memory()
-    hv = torch.from_numpy(x["v"]).pin_memory()
-    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-    qv, kv_, vv = q.view(torch.uint16), k.view(torch.uint16), v.view(torch.uint16)
+    rec = {"ms_per_step": sel_ms, "value": value, "unit": "TFLOP/s", "roofline": roofline,
+           "forward_ms_per_sequence": ms, "clocks": clk.summary(),
+           "gpu_launches": 3 * nch * steps,
+           "config": {"workload": workload_desc(w), "chunk": chunk,
+                      "l2": "K cache 134 MB per chunk call > 126 MB L2; no flush"}}
+    if e2e:
+        # end to end: the sequence's q, k, v go up from pinned host memory, out comes back
+        hq = torch.from_numpy(x["q"]).pin_memory()
+        hk = torch.from_numpy(x["k"]).pin_memory()
+        hv = torch.from_numpy(x["v"]).pin_memory()
+        hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        qv, kv_, vv = q.view(torch.uint16), k.view(torch.uint16), v.view(torch.uint16)
 
-    def e2e_step():
-        qv.copy_(hq, non_blocking=True)
-        kv_.copy_(hk, non_blocking=True)
-        vv.copy_(hv, non_blocking=True)
-        for c in range(nch):
-            qs[c].copy_(q[:, :, c * chunk:(c + 1) * chunk])
-            topo.forward(qs[c], k, v, W=w.W, topk=w.k, n=(c + 1) * chunk, scale=w.scale,
-                         out=outs[c], workspace=ws)
-        hout.copy_(out, non_blocking=True)
+        def e2e_step():
+            qv.copy_(hq, non_blocking=True)
+            kv_.copy_(hk, non_blocking=True)
+            vv.copy_(hv, non_blocking=True)
+            for c in range(nch):
+                qs[c].copy_(q[:, :, c * chunk:(c + 1) * chunk])
+                topo.forward(qs[c], k, v, W=w.W, topk=w.k, n=(c + 1) * chunk, scale=w.scale,
+                             out=outs[c], workspace=ws)
+            hout.copy_(out, non_blocking=True)
 
-    e2e_ms = timed(e2e_step, max(1, args.steps // 2))
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = hout.numel() * hout.element_size()
-    cpu = None
-    if not args.no_cpu_baseline:
-        cpu = prefill_oracle_rate(w, x, budget_s=args.cpu_budget)
+        e2e_ms = timed(e2e_step, max(1, steps // 2))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = hout.numel() * hout.element_size()
+        rec["e2e"] = {"value": flops / (e2e_ms / 1000.0) / 1e12, "unit": "TFLOP/s",
+                      "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h}
+    if cpu_budget > 0:
+        rec["cpu_baseline"] = prefill_oracle_rate(w, x, budget_s=cpu_budget)
+    return rec
+
+
+def bench_prefill(args, w: synth.Workload):
+    """The chunked prefill as the headline line (--workload prefill-64k)."""
+    import torch
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rec = measure_prefill(args, w, dev, local, steps=args.steps,
+                          cpu_budget=0.0 if args.no_cpu_baseline else args.cpu_budget)
+    if rec.get("profile"):
+        print(json.dumps(rec), flush=True)
+        return
     line = {
-        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sel_ms,
+        "metric": PREFILL_METRIC, "value": rec["value"], "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) Q/K/V, Q+=3u, sink K[0]+=6u, "
                 f"{w.planted} planted keys per KV head",
-        "config": {"workload": workload_desc(w), "chunk": chunk,
-                   "l2": "K cache 134 MB per chunk call > 126 MB L2; no flush"},
-        "forward_ms_per_sequence": ms, "roofline": roofline, "clocks": clk.summary(),
-        "e2e": {"value": flops / (e2e_ms / 1000.0) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * nch * args.steps, "cpu_baseline": cpu,
+        "config": rec["config"], "forward_ms_per_sequence": rec["forward_ms_per_sequence"],
+        "roofline": rec["roofline"], "clocks": rec["clocks"], "e2e": rec.get("e2e"),
+        "gpu_launches": rec["gpu_launches"], "cpu_baseline": rec.get("cpu_baseline"),
     }
     print(json.dumps(line), flush=True)
 
@@ -611,6 +684,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode-1m")
     ap.add_argument("--no-dense", dest="dense", action="store_false")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="headline decode line only (no batched-decode and prefill sub-records)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--n", type=int, default=0,
@@ -630,6 +705,8 @@ def main():
     w = synth.CONFIGS[WORKLOADS[args.workload]]
     if args.n:
         w = w.with_(n=args.n, name=f"{w.name} (n overridden to {args.n})")
+    if args.profile or args.n:
+        args.workloads = False
     if args.profile:
         args.dense = False
         args.no_cpu_baseline = True

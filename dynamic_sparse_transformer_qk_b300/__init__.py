@@ -25,9 +25,9 @@ import threading
 
 import torch
 
-__all__ = ["forward", "forward_noalloc", "score_select", "sparse_softmax_pv", "dense_forward", "Workspace",
-           "TopoError", "library_path", "load_library", "workspace_size", "dense_workspace_size",
-           "device_status", "EXPORTS"]
+__all__ = ["forward", "forward_noalloc", "score_select", "sparse_softmax_pv", "dense_forward",
+           "layer_schedule", "layers_forward", "Workspace", "TopoError", "library_path",
+           "load_library", "workspace_size", "dense_workspace_size", "device_status", "EXPORTS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "libtopoattn.so")
@@ -38,7 +38,8 @@ _lib = None
 EXPORTS = ("topo_attn_workspace_size", "dense_attn_workspace_size", "topo_attn_workspace_init",
            "topo_attn_forward", "topo_attn_score_select", "topo_attn_sparse_softmax_pv",
            "dense_attn_forward", "topo_attn_strerror", "topo_attn_device_status",
-           "topo_attn_forward_noalloc")
+           "topo_attn_forward_noalloc", "topo_attn_layer_schedule",
+           "topo_attn_layers_workspace_size", "topo_attn_layers_forward")
 
 TOPO_OK = 0
 TOPO_KMAX = 256
@@ -55,6 +56,13 @@ class Params(ctypes.Structure):
                 ("d", ctypes.c_int32), ("n", ctypes.c_int64), ("nq", ctypes.c_int64),
                 ("kv_stride", ctypes.c_int64), ("W", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class TopoLayer(ctypes.Structure):
+    """One layer of topo_attn_layers_forward (include/topo_attn.h)."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("W", ctypes.c_int32), ("k_top", ctypes.c_int32),
+                ("dense", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -84,6 +92,10 @@ def load_library():
             "topo_attn_strerror": (ctypes.c_char_p, [i]),
             "topo_attn_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
             "topo_attn_forward_noalloc": (i, [P, vp, vp, vp, vp, vp, vp, vp]),
+            "topo_attn_layer_schedule": (i, [ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int32,
+                                             ctypes.c_int32, vp]),
+            "topo_attn_layers_workspace_size": (sz, [P, vp, ctypes.c_int32]),
+            "topo_attn_layers_forward": (i, [P, vp, ctypes.c_int32, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -297,6 +309,54 @@ def forward_noalloc(q, k, v, *, W: int, topk: int, n: int | None = None,
                                            _stream(stream, q.device))
     _raise(rc, "topo_attn_forward_noalloc")
     return out, idx, excl
+
+
+def layer_schedule(L: int, *, pillar_every: int = 16, windows=(256, 128, 64),
+                   topk: int = 32) -> list:
+    """The per-layer settings topo_attn_layer_schedule assigns: a list of L
+    dicts {"W", "topk", "dense"} (pillar layers every `pillar_every` layers
+    from layer 0; sparse layers take `windows` by depth tier, widest first)."""
+    lib = load_library()
+    arr = (TopoLayer * L)() if L > 0 else None
+    win = (ctypes.c_int32 * len(windows))(*windows)
+    rc = lib.topo_attn_layer_schedule(L, pillar_every, ctypes.addressof(win), len(windows),
+                                      topk, ctypes.addressof(arr) if arr is not None else None)
+    _raise(rc, "topo_attn_layer_schedule")
+    return [{"W": a.W, "topk": a.k_top, "dense": bool(a.dense)} for a in arr]
+
+
+def layers_forward(qs, ks, vs, schedule, *, n: int | None = None, scale: float | None = None,
+                   outs=None, workspace: Workspace | None = None, stream=None):
+    """topo_attn_layers_forward: layer l attends with its own q, k, v and
+    schedule[l] (a dict as from layer_schedule); returns the list of outputs."""
+    L = len(schedule)
+    if not (len(qs) == len(ks) == len(vs) == L) or L < 1:
+        raise ValueError("one q, k, v and schedule entry per layer")
+    for q, k, v in zip(qs, ks, vs):
+        _check(q, k, v)
+        if q.shape != qs[0].shape or k.shape != ks[0].shape or v.shape != ks[0].shape \
+                or q.dtype != qs[0].dtype or q.device != qs[0].device:
+            raise ValueError("every layer must have the same shapes, dtype and device")
+    lib = load_library()
+    q0 = qs[0]
+    p = make_params(q0, ks[0], W=1, topk=0, n=n, scale=scale)
+    B, Hq, nq, d = q0.shape
+    if outs is None:
+        outs = [torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q0.device)
+                for _ in range(L)]
+    arr = (TopoLayer * L)()
+    for a, q, k, v, o, sch in zip(arr, qs, ks, vs, outs, schedule):
+        a.q, a.k, a.v, a.out = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+        a.W, a.k_top, a.dense, a.reserved = int(sch["W"]), int(sch["topk"]), int(sch["dense"]), 0
+    need = int(lib.topo_attn_layers_workspace_size(ctypes.byref(p), ctypes.addressof(arr), L))
+    if need == 0:
+        _raise(-1 if p.d in (64, 128) else -2, "topo_attn_layers_workspace_size")
+    ws = _workspace(workspace, q0.device, need, stream)
+    with torch.cuda.device(q0.device):
+        rc = lib.topo_attn_layers_forward(ctypes.byref(p), ctypes.addressof(arr), L, ws.ptr,
+                                          ws.nbytes, _stream(stream, q0.device))
+    _raise(rc, "topo_attn_layers_forward")
+    return outs
 
 
 def device_status(ws: Workspace, stream=None) -> int:

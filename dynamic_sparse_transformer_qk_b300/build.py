@@ -61,9 +61,14 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _headers():
+    return (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+            + [os.path.abspath(__file__)])
+
+
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    deps = [src] + _deps()
+    deps = [src] + _headers()  # a unit depends on its own source and the shared headers
     if _stale(obj, deps):
         cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj + ".tmp"]
         if verbose:

@@ -122,22 +122,11 @@ int stages_for(int stage_bytes, int fixed_bytes, int min_ring) {
   return st;
 }
 
-// Ring depth and consumer-warp count of the CUDA-core kernels.  Consumer warp
-// w takes tiles w, w + ncw, ... and tile t uses stage t % stages, so ncw must
-// divide the depth: then a stage is only ever read by one warp, and its
-// previous fill was that warp's own, already consumed (the parity-only
-// barrier wait is unambiguous).  All four warps are used whenever the ring
-// can be rounded down to a multiple of four and still hold `min_ring` bytes.
+// Ring depth and consumer-warp count of the CUDA-core kernels: the consumer
+// count may not exceed the depth (see consume_tiles for why).
 void ring_shape(int stage_bytes, int fixed_bytes, int min_ring, int* stages, int* ncw) {
-  int st = stages_for(stage_bytes, fixed_bytes, min_ring);
-  const int w4 = topo::kConsumerWarps;
-  if (st >= w4 && (st - st % w4) * stage_bytes >= min_ring) {
-    *stages = st - st % w4;
-    *ncw = w4;
-    return;
-  }
-  *stages = st;
-  *ncw = st % 3 == 0 ? 3 : (st % 2 == 0 ? 2 : 1);
+  *stages = stages_for(stage_bytes, fixed_bytes, min_ring);
+  *ncw = *stages < topo::kConsumerWarps ? *stages : topo::kConsumerWarps;
 }
 
 // Plan for the condensate-set passes (dense=false) or the dense pass.
@@ -320,6 +309,15 @@ Geom base_geom(const topo_attn_params* p, const Plan& P) {
   return G;
 }
 
+// The parameters of one layer of a multi-layer step: the shared shapes of
+// `p` with the layer's own window and top-k (a pillar layer ignores both).
+topo_attn_params layer_params(const topo_attn_params* p, const topo_layer& l) {
+  topo_attn_params q = *p;
+  q.W = l.dense ? 1 : l.W;
+  q.k = l.dense ? 0 : l.k_top;
+  return q;
+}
+
 int to_status(cudaError_t e) {
   if (e == cudaSuccess) return TOPO_OK;
   return TOPO_ERR_CUDA;
@@ -498,6 +496,63 @@ int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, 
   rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_part - P.off_cnt, st));
   if (rc != TOPO_OK) return rc;
   return dispatch(P.bf16, P.D, [&](auto L) { return L.dense(P.NC, mk, mv, G, grid, P.smem, st); });
+}
+
+int topo_attn_layer_schedule(int32_t L, int32_t pillar_every, const int32_t* windows,
+                             int32_t n_windows, int32_t k, topo_layer* layers) {
+  if (L < 1 || n_windows < 1 || !windows || !layers || k < 0 || k > TOPO_KMAX ||
+      pillar_every < 0)
+    return TOPO_ERR_INVALID_ARG;
+  for (int i = 0; i < n_windows; ++i)
+    if (windows[i] < 1) return TOPO_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l) {
+    layers[l].dense = (pillar_every > 0 && l % pillar_every == 0) ? 1 : 0;
+    layers[l].W = windows[(long long)l * n_windows / L];
+    layers[l].k_top = k;
+    layers[l].reserved = 0;
+  }
+  return TOPO_OK;
+}
+
+size_t topo_attn_layers_workspace_size(const topo_attn_params* p, const topo_layer* layers,
+                                       int32_t L) {
+  if (!p || !layers || L < 1) return 0;
+  size_t need = 256;
+  for (int l = 0; l < L; ++l) {
+    const topo_attn_params lp = layer_params(p, layers[l]);
+    Plan P;
+    if (make_plan(&lp, layers[l].dense != 0, &P) != TOPO_OK) return 0;
+    need = P.total > need ? P.total : need;
+  }
+  return need;
+}
+
+int topo_attn_layers_forward(const topo_attn_params* p, const topo_layer* layers, int32_t L,
+                             void* ws, size_t ws_bytes, topo_stream_t stream) {
+  if (!p || !layers || L < 1) return TOPO_ERR_INVALID_ARG;
+  // every layer is checked before the first one is enqueued
+  for (int l = 0; l < L; ++l) {
+    const topo_layer& ly = layers[l];
+    const topo_attn_params lp = layer_params(p, ly);
+    Plan P;
+    const int rc = make_plan(&lp, ly.dense != 0, &P);
+    if (rc != TOPO_OK) return rc;
+    if (ly.reserved != 0 || !ly.q || !ly.k || !ly.v || !ly.out) return TOPO_ERR_INVALID_ARG;
+    if (!aligned16(ly.q) || !aligned16(ly.k) || !aligned16(ly.v)) return TOPO_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < P.total)
+      return TOPO_ERR_WORKSPACE;
+  }
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  for (int l = 0; l < L; ++l) {
+    const topo_layer& ly = layers[l];
+    const topo_attn_params lp = layer_params(p, ly);
+    const int rc = ly.dense ? dense_attn_forward(&lp, ly.q, ly.k, ly.v, ly.out, ws, ws_bytes,
+                                                 stream)
+                            : run_topo(&lp, ly.q, ly.k, ly.v, ly.out, nullptr, nullptr, ws,
+                                       ws_bytes, st);
+    if (rc != TOPO_OK) return rc;
+  }
+  return TOPO_OK;
 }
 
 const char* topo_attn_strerror(int status) {

@@ -42,7 +42,7 @@ struct Geom {
   long long hi_units;     // units that use L2 (one more split each); 0: none
   int nsplit_max;         // grid.x = ncb * nsplit_max
   int stages;             // ring depth
-  int ncw;                // consumer warps that score tiles (1..kConsumerWarps; divides stages)
+  int ncw;                // consumer warps that score tiles (1..kConsumerWarps, <= stages)
   int flags;
   const void* qp;
   const void* kp;
@@ -304,11 +304,15 @@ __device__ __forceinline__ void drain_tiles(int issued, int stages, uint64_t* fu
   }
 }
 
-// Consumer loop of warp `warp` (< ncw): tiles warp, warp+ncw, ...;
-// body(t, stage_ptr).  ncw divides `stages`, so every stage is only ever read
-// by one warp and tile t - stages (the previous fill of t's stage) is this
-// warp's own, already consumed: the parity wait below cannot match a phase two
-// fills old.  Warps >= ncw take no tiles.
+// Consumer loop of warp `warp` (< ncw <= stages): tiles warp, warp+ncw, ...;
+// body(t, stage_ptr).  Tile t fills stage s = t % stages for the R-th time
+// (R = t / stages).  A parity wait alone cannot tell fill R from fill R-2, and
+// another warp may still hold fill R-1 of the stage, so the warp first waits
+// until fill R-1 has been consumed (phase R-1 of empty[s]), then for fill R to
+// land (phase R of full[s]).  The first wait is unambiguous because the
+// producer issued tile t - stages (<= this warp's previous tile, as ncw <=
+// stages) only after tile t - 2 stages had been consumed, and the second
+// because tile t itself is not consumed yet.  Warps >= ncw take no tiles.
 template <class Body>
 __device__ __forceinline__ void consume_tiles(int warp, int ncw, int ntiles, int stages,
                                               int stage_bytes, uint8_t* ring, uint64_t* full,
@@ -319,7 +323,8 @@ __device__ __forceinline__ void consume_tiles(int warp, int ncw, int ntiles, int
   for (int t = warp; t < ntiles; t += ncw) {
     const int s = t % stages;
     const uint32_t round = (uint32_t)(t / stages);
-    const bool ok = __all_sync(kFull, mbar_wait(&full[s], round & 1u));
+    const bool ok = __all_sync(kFull, (round == 0u || mbar_wait(&empty[s], (round - 1u) & 1u)) &&
+                                          mbar_wait(&full[s], round & 1u));
     const int ab = __shfl_sync(kFull, *abort_flag, 0);
     if (!ok || ab) {
       if (!ok && lane == 0) {

@@ -142,6 +142,60 @@ int dense_attn_forward(const topo_attn_params *p, const void *q, const void *k, 
                        float *out, void *ws, size_t ws_bytes, topo_stream_t stream);
 
 /*
+ * Multi-layer step with layer-adaptive sets and pillar layers [zh S3,
+ * "implementation strategy": early layers use wider windows, later layers
+ * leaner sets, and a few layers (e.g. L/16) keep full attention so that
+ * global information still flows; ko S3, "layer-adaptive configuration"].
+ *
+ * One topo_layer per layer: that layer's own q, k, v and out (layouts and
+ * alignment as for topo_attn_forward), its window W and top-k k, and whether
+ * it is a pillar (dense != 0: dense_attn_forward, W and k ignored).
+ */
+typedef struct {
+  const void *q;      /* [B, Hq, nq, d] */
+  const void *k;      /* [B, Hkv, kv_stride, d] */
+  const void *v;      /* [B, Hkv, kv_stride, d] */
+  float *out;         /* [B, Hq, nq, d] float32 */
+  int32_t W;          /* window of a sparse layer, >= 1 */
+  int32_t k_top;      /* top-k of a sparse layer, 0 <= k_top <= TOPO_KMAX */
+  int32_t dense;      /* nonzero: pillar layer (full causal attention) */
+  int32_t reserved;   /* set to 0 */
+} topo_layer;
+
+/*
+ * Fill the W, k_top and dense fields of layers[0..L) with the schedule this
+ * library reads from the pages (they fix no numbers beyond "e.g. L/16"):
+ *   - layer l is a pillar when pillar_every > 0 and l % pillar_every == 0
+ *     (pillar_every = 16 gives L/16 pillars, the first at layer 0);
+ *   - the sparse layers take their window from `windows` (n_windows values,
+ *     widest first) by depth tier: layer l uses windows[l * n_windows / L];
+ *   - every sparse layer uses top-k `k`.
+ * Pointers in layers[] are left as they are.  Returns TOPO_ERR_INVALID_ARG for
+ * L < 1, n_windows < 1, a window < 1, k outside 0..TOPO_KMAX or pillar_every < 0.
+ */
+int topo_attn_layer_schedule(int32_t L, int32_t pillar_every, const int32_t *windows,
+                             int32_t n_windows, int32_t k, topo_layer *layers);
+
+/* Workspace bytes for topo_attn_layers_forward: the largest need of any
+ * layer (layers run one after another on the stream and share it); 0 if
+ * any layer is invalid or unsupported. */
+size_t topo_attn_layers_workspace_size(const topo_attn_params *p, const topo_layer *layers,
+                                       int32_t L);
+
+/*
+ * Run L layers in order on `stream`: layer l computes condensate-set
+ * attention (topo_attn_forward with its own W and k_top) or, for a pillar,
+ * dense causal attention, on its own q, k, v into its own out.  `p` gives the
+ * shapes every layer shares (B, Hq, Hkv, d, n, nq, kv_stride, scale, dtype);
+ * its W and k are ignored.  Every layer is checked before anything is
+ * enqueued, so an argument error enqueues no work.  The layers' inputs are
+ * independent here: a model would compute layer l+1's q, k, v from layer l's
+ * out between the layers, which is outside this library.
+ */
+int topo_attn_layers_forward(const topo_attn_params *p, const topo_layer *layers, int32_t L,
+                             void *ws, size_t ws_bytes, topo_stream_t stream);
+
+/*
  * topo_attn_forward without a caller-supplied workspace.  (The paper has no
  * counterpart; this is a deployment convenience of this library.)
  *

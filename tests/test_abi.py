@@ -106,3 +106,62 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 1, 64)
     with pytest.raises(ValueError):
         topo.forward(q, q, q, W=4, topk=2)
+
+
+# ------------------------------------------------------ multi-layer step ----
+
+def test_layer_schedule_pillars_and_window_tiers():
+    """32 layers, a pillar every 16 (L/16 = 2 pillars, at 0 and 16), windows
+    256 / 128 / 64 by depth third, k = 32 everywhere."""
+    sch = topo.layer_schedule(32, pillar_every=16, windows=(256, 128, 64), topk=32)
+    assert [l for l, s in enumerate(sch) if s["dense"]] == [0, 16]
+    assert [s["W"] for s in sch] == [256] * 11 + [128] * 11 + [64] * 10
+    assert all(s["topk"] == 32 for s in sch)
+    ws = [s["W"] for s in sch if not s["dense"]]
+    assert ws == sorted(ws, reverse=True)          # wide early, narrow late
+    assert not any(s["dense"] for s in topo.layer_schedule(5, pillar_every=0))
+    assert [s["W"] for s in topo.layer_schedule(3, windows=(9,))] == [9, 9, 9]
+
+
+def test_layer_schedule_rejects_bad_arguments(lib):
+    arr = (topo.TopoLayer * 4)()
+    win = (ctypes.c_int32 * 2)(64, 32)
+    a, w = ctypes.addressof(arr), ctypes.addressof(win)
+    assert lib.topo_attn_layer_schedule(4, 2, w, 2, 8, a) == 0
+    assert [x.dense for x in arr] == [1, 0, 1, 0] and [x.W for x in arr] == [64, 64, 32, 32]
+    assert lib.topo_attn_layer_schedule(0, 2, w, 2, 8, a) == -1
+    assert lib.topo_attn_layer_schedule(4, -1, w, 2, 8, a) == -1
+    assert lib.topo_attn_layer_schedule(4, 2, w, 0, 8, a) == -1
+    assert lib.topo_attn_layer_schedule(4, 2, w, 2, 300, a) == -1
+    assert lib.topo_attn_layer_schedule(4, 2, None, 2, 8, a) == -1
+    bad = (ctypes.c_int32 * 2)(64, 0)
+    assert lib.topo_attn_layer_schedule(4, 2, ctypes.addressof(bad), 2, 8, a) == -1
+
+
+def test_layers_forward_checks_every_layer_first(lib):
+    p = _p()
+    arr = (topo.TopoLayer * 3)()
+    for x in arr:
+        x.q = x.k = x.v = x.out = FAKE
+        x.W, x.k_top, x.dense = 64, 32, 0
+    arr[1].dense = 1
+    a = ctypes.addressof(arr)
+    need = lib.topo_attn_layers_workspace_size(ctypes.byref(p), a, 3)
+    assert need >= max(lib.topo_attn_workspace_size(ctypes.byref(p)),
+                       lib.dense_attn_workspace_size(ctypes.byref(p)))
+    # a bad last layer: nothing is enqueued for the good ones before it
+    arr[2].out = None
+    assert lib.topo_attn_layers_forward(ctypes.byref(p), a, 3, FAKE, need, None) == -1
+    arr[2].out = FAKE
+    arr[2].k_top = 999
+    assert lib.topo_attn_layers_forward(ctypes.byref(p), a, 3, FAKE, need, None) == -2
+    assert lib.topo_attn_layers_workspace_size(ctypes.byref(p), a, 3) == 0
+    arr[2].k_top = 32
+    arr[0].reserved = 1
+    assert lib.topo_attn_layers_forward(ctypes.byref(p), a, 3, FAKE, need, None) == -1
+    arr[0].reserved = 0
+    assert lib.topo_attn_layers_forward(ctypes.byref(p), a, 3, FAKE, need - 1, None) == -3
+    assert lib.topo_attn_layers_forward(ctypes.byref(p), a, 0, FAKE, need, None) == -1
+    # a pillar layer ignores W and k: a bad W there is not an error
+    arr[1].W = -5
+    assert lib.topo_attn_layers_workspace_size(ctypes.byref(p), a, 3) == need
