@@ -239,7 +239,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
     if (P->pf) {
       const size_t ncolumns = (size_t)p->B * p->Hkv * P->ncols;
       P->off_surv = o;
-      o = align256(o + ncolumns * topo::kPfLL * 4);
+      o = align256(o + ncolumns * topo::kPfLL * 8);
       P->off_scnt = o;
       o = align256(o + ncolumns * 4);
       P->off_topk = o;
@@ -376,7 +376,7 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
     if (rc != TOPO_OK) return rc;
     G.kmax = reinterpret_cast<unsigned*>(w + P.off_kmax);
     G.work = reinterpret_cast<int*>(w + P.off_work);
-    G.surv = reinterpret_cast<unsigned*>(w + P.off_surv);
+    G.surv = reinterpret_cast<float2*>(w + P.off_surv);
     G.surv_cnt = reinterpret_cast<int*>(w + P.off_scnt);
     G.topsel = reinterpret_cast<int*>(w + P.off_topk);
     G.nitems = P.pf_nitems;

@@ -57,7 +57,7 @@ struct Geom {
   float* partials;        // [unit][split][NC][...]
   // chunked-prefill tensor-core path (topo_prefill.cuh)
   unsigned* kmax;             // [B*Hkv] float bits of the largest |k_c| over keys 0..n-1
-  unsigned* surv;             // [column][kPfLL] surviving candidates (packed)
+  float2* surv;               // [column][kPfLL] surviving candidates (tensor-core score, position bits)
   int* surv_cnt;              // [column] survivors, -1 when the buffer overflowed
   int* work;                  // work-queue counter of the scan kernel
   int* topsel;                // [row][k] selected positions ascending, -1 padded

@@ -16,26 +16,33 @@
 //   prefill_scan_kernel      persistent; one work item = 128 query columns
 //                            (query row x head pairs of one KV head) against
 //                            all their candidate keys, 256 keys per tile, in
-//                            two passes (pass 1 finds each column's starting
-//                            cut from the maxima of every second tile):
-//                            M = 128 columns (A: queries, resident in shared
-//                            memory), N = 256 keys (B: K tile by TMA), the
-//                            accumulator in TMEM (two buffers).  Each epilogue
-//                            thread owns one column: it keeps a candidate
-//                            buffer in shared memory, appends every score
-//                            above the column's cut and, when a buffer fills,
+//                            two passes over the same tiles: M = 128 columns
+//                            (A: queries, resident in shared memory), N = 256
+//                            keys (B: K tile by TMA), the accumulator in TMEM
+//                            (two buffers).  Each epilogue thread owns one
+//                            column.  Pass 1 offers only the maxima of groups
+//                            of keys (whole 128-key halves of a tile for long
+//                            items, down to 8-key groups for short ones) to
+//                            the column's candidate buffer; their k-th
+//                            largest U bounds the column's k-th best
+//                            tensor-core score from below (k distinct keys
+//                            reach it), so U - 2 delta starts pass 2's cut
+//                            (delta: the bound on |tensor core - exact chain|,
+//                            see topo_tc_kernels.cuh).  Pass 2 appends every
+//                            score above the cut and, when a buffer fills,
 //                            the warp compacts that column (a bisection on
-//                            warp-wide counts): the cut becomes T - 2 delta,
-//                            T at most the column's k-th best tensor-core
-//                            score and delta the bound on |tensor core - exact
-//                            chain| (see topo_tc_kernels.cuh).  Survivors go to
-//                            the workspace;
-//   prefill_finalize_kernel  one warp per column: rescores the survivors with
-//                            the exact chain, keeps the exact top-k (ties to
-//                            the lower position) and writes the sorted top-k,
-//                            C_i (idx) and the k-th key for the excluded-mass
-//                            pass.  A column whose near ties overflowed its
-//                            buffer is rescanned exactly on CUDA cores;
+//                            warp-wide counts), raising the cut.  Survivors,
+//                            with their tensor-core scores, go to the
+//                            workspace;
+//   prefill_finalize_kernel  one warp per column: the exact top-k (ties to the
+//                            lower position) from the survivors.  Survivors
+//                            whose tensor-core score clears the boundary by
+//                            2 delta are in without rescoring; the others are
+//                            rescored with the exact chain.  Writes the sorted
+//                            top-k, C_i (idx) and, when the excluded mass is
+//                            requested, the exact k-th key.  A column whose
+//                            near ties overflowed its buffer is rescanned
+//                            exactly on CUDA cores;
 //   prefill_pv_kernel        one warp per row: float32 online softmax over
 //                            C_i and the weighted sum of V.
 #pragma once
@@ -54,8 +61,7 @@ constexpr int kPfSub = 8;      // scores offered between room checks
 constexpr int kPfLL = 64;      // survivors published per column
 constexpr int kPfStride = kPfCols + 1;  // buffer row stride (entries)
 constexpr int kPfEpiWarps = 4; // one per TMEM lane quarter
-constexpr int kPfP1Stride = 2; // the first pass reads every kPfP1Stride-th tile
-constexpr int kPfAcc = 2;      // TMEM accumulator buffers (kPfKeys columns each)
+constexpr int kPfAcc = 2;      // TMEM accumulator buffers (kPfKeys columns each: all 512)
 constexpr int kPfWarps = 2 + kPfEpiWarps;  // + TMA producer + MMA issuer
 constexpr int kPfThreads = 32 * kPfWarps;
 
@@ -98,7 +104,6 @@ __global__ void __launch_bounds__(256) prefill_kmax_kernel(const Geom G) {
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) f = fmaxf(f, red[w]);
-    f = fmaxf(f, red[0]);
     atomicMax(G.kmax + bh, __float_as_uint(f));  // non-negative floats order as integers
   }
 }
@@ -200,17 +205,21 @@ static __device__ __noinline__ PfState pf_compact_lane(float2* be, int cl, int k
                                                        bool hold) {
   const int n = st.cnt;
   if (st.ovf || kk <= 0 || n < kk || n < at_least) return st;
+  // the column's scores in registers (absent slots -inf), then the bisection
+  float v[kPfCap];
   float lo = INFINITY, hi = -INFINITY;
-  for (int i = 0; i < n; ++i) {
-    const float v = be[i * kPfStride + cl].x;
-    lo = fminf(lo, v);
-    hi = fmaxf(hi, v);
+#pragma unroll
+  for (int i = 0; i < kPfCap; ++i) {
+    v[i] = i < n ? be[i * kPfStride + cl].x : -INFINITY;
+    lo = i < n ? fminf(lo, v[i]) : lo;
+    hi = fmaxf(hi, v[i]);
   }
 #pragma unroll 1
   for (int it = 0; it < 10; ++it) {
     const float mid = 0.5f * (lo + hi);
     int c = 0;
-    for (int i = 0; i < n; ++i) c += be[i * kPfStride + cl].x >= mid ? 1 : 0;
+#pragma unroll
+    for (int i = 0; i < kPfCap; ++i) c += v[i] >= mid ? 1 : 0;
     if (c >= kk) lo = mid;
     else hi = mid;
   }
@@ -228,16 +237,6 @@ static __device__ __noinline__ PfState pf_compact_lane(float2* be, int cl, int k
     if (!hold) st.thr = INFINITY;
   }
   return st;
-}
-
-__device__ __forceinline__ float max64(const float (&a)[32], const float (&b)[32]) {
-  float m[8];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    m[s] = max8(a + 8 * s);
-    m[4 + s] = max8(b + 8 * s);
-  }
-  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 // Offer 64 consecutive scores (positions jg..jg+63) of this thread's column,
@@ -266,14 +265,32 @@ __device__ __forceinline__ void pf_offer64(const float (&sa)[32], const float (&
     }
     const float* v = s < 4 ? sa + 8 * s : sb + 8 * (s - 4);
     const int j0 = (int)(jg + 8 * s);
-    int n = st.ovf ? 0 : st.cnt;  // an overflowed column only scribbles on its slot 0
+    // the group's candidates go to consecutive free slots: the eight compares
+    // first, then each slot from a prefix count (independent stores)
+    unsigned bits = 0u;
+#pragma unroll
+    for (int i = 0; i < kPfSub; ++i) bits |= (v[i] > st.thr) ? (1u << i) : 0u;
+    if (st.ovf) bits = 0u;
+    const int n = st.cnt;
 #pragma unroll
     for (int i = 0; i < kPfSub; ++i) {
-      be[n * kPfStride + cl] = make_float2(v[i], __int_as_float(j0 + i));
-      n += v[i] > st.thr ? 1 : 0;
+      if (bits & (1u << i))
+        be[(n + __popc(bits & ((1u << i) - 1u))) * kPfStride + cl] =
+            make_float2(v[i], __int_as_float(j0 + i));
     }
-    if (!st.ovf) st.cnt = n;
+    const int nn = n + __popc(bits);
+    st.cnt = nn;
   }
+}
+
+__device__ __forceinline__ float max64(const float (&a)[32], const float (&b)[32]) {
+  float m[8];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    m[s] = max8(a + 8 * s);
+    m[4 + s] = max8(b + 8 * s);
+  }
+  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 template <int D>
@@ -319,7 +336,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
 
-  long long seq = 0;  // tiles this CTA has run (phases of the ring and accumulator barriers)
+  long long seq = 0;     // tiles this CTA has run (phases of the ring and accumulator barriers)
+  long long issued = 0;  // tiles the producer has issued (equals seq unless aborted)
   for (;;) {
     __syncthreads();
     if (tid == 0) misc[2] = atomicAdd(G.work, 1);
@@ -336,8 +354,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const long long r_last = (cend - 1) / G.g;
     const long long jmax = G.n - G.nq + r_last - G.W;
     const int ntiles = jmax >= 1 ? (int)((jmax + kPfKeys - 1) / kPfKeys) : 0;
-    // pass 1 reads tiles 0, S, 2S, ... (S = kPfP1Stride); pass 2 every tile
-    const int n1 = (ntiles + kPfP1Stride - 1) / kPfP1Stride;
     const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
 
     // queries of the block: bf16, K-major, 128-byte swizzle; missing columns zero
@@ -364,7 +380,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // ring slot and round of tile seq + t, advanced without a division per tile
         int s = (int)(seq % stages);
         uint32_t round = (uint32_t)(seq / stages);
-        for (int t = 0; t < n1 + ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
+        for (int t = 0; t < 2 * ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
                  round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
           if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
@@ -374,7 +390,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           uint8_t* dst = ring + (size_t)s * TILEB;
           mbar_arrive_expect_tx(&full[s], (uint32_t)TILEB);
-          const int tt = t < n1 ? t * kPfP1Stride : t - n1;
+          ++issued;
+          const int tt = t < ntiles ? t : t - ntiles;  // both passes run the same tiles
           const int y = (int)(kvrow0 + 1 + (long long)tt * kPfKeys);
 #pragma unroll
           for (int cc = 0; cc < S::NCH; ++cc)
@@ -391,7 +408,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const uint64_t bdesc0 = tc::smem_desc_sw128(smem_addr(ring));
         int s = (int)(seq % stages);
         uint32_t round = (uint32_t)(seq / stages);
-        for (int t = 0; t < n1 + ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
+        for (int t = 0; t < 2 * ntiles; ++t, s = (s + 1 == stages) ? 0 : s + 1,
                  round += (s == 0) ? 1u : 0u) {
           if (misc[0]) break;
           const long long gs = seq + t;
@@ -436,17 +453,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float kmx = __uint_as_float(G.kmax[bh]);
       const float two_delta = 2.f * tc_delta_factor(D) * qn1 * 1.001f * kmx;
       PfState st{0, -INFINITY, 0};
+      // pass-1 values per 128 keys: enough group maxima (>= 4k) per column
+      int vpt = 1;
+      while (vpt < 16 && vpt * ntiles * (kPfKeys / kPfSubKeys) < 4 * kk) vpt <<= 1;
       const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
-      // Pass 1 (t < n1) offers only the largest score of each of its tiles
-      // (every kPfP1Stride-th tile, one value per 256 keys); the k-th largest
-      // such maximum U is a lower bound of the column's k-th best tensor-core
-      // score (k distinct keys reach it, whichever tiles they came from), so
-      // U - 2 delta is a valid starting cut for pass 2, which offers every
-      // score of every tile.  Both passes compute the same scores for a tile
-      // (identical operands and instruction sequence).
-      for (int t = 0; t < n1 + ntiles; ++t) {
-        const bool p1 = t < n1;
-        if (t == n1) {
+      for (int t = 0; t < 2 * ntiles; ++t) {
+        const bool p1 = t < ntiles;
+        if (t == ntiles) {
+          // U from the pass-1 group maxima (k distinct keys reach it)
           st = pf_compact_lane(be, cl, kk, two_delta, st, 0, 0, true);
           st.cnt = 0;
           st.ovf = 0;
@@ -463,15 +477,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const int tt = p1 ? t * kPfP1Stride : t - n1;
-        const long long j0 = 1 + (long long)tt * kPfKeys;
-        float bm = -INFINITY;
+        const int tt = p1 ? t : t - ntiles;
 #pragma unroll 1
         for (int sub = 0; sub < kPfKeys / kPfSubKeys; ++sub) {
-          // 128 scores of this column in registers; after the last read the
-          // accumulator goes straight back to the MMA issuer
+          const long long js = 1 + (long long)tt * kPfKeys + sub * kPfSubKeys;
+          // 128 scores of this column in registers; after the last read of the
+          // tile the accumulator goes straight back to the MMA issuer
           float sa[32], sb[32], sc[32], sd[32];
-          const long long js = j0 + sub * kPfSubKeys;
           {
             const uint32_t ta = tq + (uint32_t)(ab * kPfKeys + sub * kPfSubKeys);
             tc::tmem_ld16(ta, *reinterpret_cast<float(*)[16]>(sa));
@@ -498,35 +510,51 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               if (js + 96 + i > jhi) sd[i] = -INFINITY;
             }
           }
-          if (p1) {
-            bm = fmaxf(bm, fmaxf(max64(sa, sb), max64(sc, sd)));
-          } else {
-            // the maxima of the sixteen 8-score groups (independent), then one
-            // vote: most steps hold no candidate for any column of the warp
-            float m[16];
+          // the maxima of the sixteen 8-score groups (independent)
+          float m[16];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              m[g] = max8(sa + 8 * g);
-              m[4 + g] = max8(sb + 8 * g);
-              m[8 + g] = max8(sc + 8 * g);
-              m[12 + g] = max8(sd + 8 * g);
-            }
-            const float mt = fmaxf(max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]),
-                                         max3f(m[6], m[7], m[8])),
-                                   max3f(max3f(m[9], m[10], m[11]), max3f(m[12], m[13], m[14]),
-                                         m[15]));
-            if (__any_sync(kFull, mt > st.thr)) {
-              pf_offer64(sa, sb, m, js, be, quarter, lane, cl, kk, two_delta, st);
-              pf_offer64(sc, sd, m + 8, js + 64, be, quarter, lane, cl, kk, two_delta, st);
-            }
+          for (int g = 0; g < 4; ++g) {
+            m[g] = max8(sa + 8 * g);
+            m[4 + g] = max8(sb + 8 * g);
+            m[8 + g] = max8(sc + 8 * g);
+            m[12 + g] = max8(sd + 8 * g);
           }
-        }
-        if (p1) {
-          if (__any_sync(kFull, !st.ovf && st.cnt >= kPfCap))
-            st = pf_compact_lane(be, cl, kk, two_delta, st, 0, 1, true);
-          if (!st.ovf && bm > st.thr) {
-            be[st.cnt * kPfStride + cl] = make_float2(bm, __int_as_float(tt));
-            ++st.cnt;
+          if (p1) {
+            // the maxima of 128 / vpt-key groups (distinct keys), offered to
+            // the buffer; their kk-th largest bounds the column's kk-th best
+            float gm[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) gm[i] = m[i];
+#pragma unroll
+            for (int l = 0; l < 4; ++l) {
+              if ((16 >> l) > vpt) {
+#pragma unroll
+                for (int i = 0; i < (8 >> l); ++i) gm[i] = fmaxf(gm[2 * i], gm[2 * i + 1]);
+              }
+            }
+            if (__any_sync(kFull, !st.ovf && st.cnt + vpt > kPfCap))
+              st = pf_compact_lane(be, cl, kk, two_delta, st, 0, vpt, true);
+            if (!st.ovf) {
+              int n = st.cnt;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                if (i < vpt) {
+                  be[n * kPfStride + cl] = make_float2(gm[i], __int_as_float((int)js));
+                  n += gm[i] > st.thr ? 1 : 0;
+                }
+              }
+              st.cnt = n;
+            }
+            continue;
+          }
+          // one vote: most steps hold no candidate for any column of the warp
+          const float mt = fmaxf(max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]),
+                                       max3f(m[6], m[7], m[8])),
+                                 max3f(max3f(m[9], m[10], m[11]), max3f(m[12], m[13], m[14]),
+                                       m[15]));
+          if (__any_sync(kFull, mt > st.thr)) {
+            pf_offer64(sa, sb, m, js, be, quarter, lane, cl, kk, two_delta, st);
+            pf_offer64(sc, sd, m + 8, js + 64, be, quarter, lane, cl, kk, two_delta, st);
           }
         }
       }
@@ -540,22 +568,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int cnt_c = __shfl_sync(kFull, st.cnt, c);
         const bool ov_c = __shfl_sync(kFull, st.ovf, c) != 0;
         const long long gcol = (long long)bh * G.ncols + c0 + cc;
-        unsigned* dst = G.surv + gcol * kPfLL;
+        float2* dst = G.surv + gcol * kPfLL;
         const bool ovl = ov_c || cnt_c > kPfLL;  // more survivors than slots: exact rescan
 #pragma unroll
         for (int r = 0; r < kPfLL / 32; ++r) {
           const int ee = lane + 32 * r;
-          dst[ee] = ee < cnt_c ? (uint32_t)(__float_as_int(be[ee * kPfStride + cc].y) - 1) : 0u;
+          if (ee < cnt_c) dst[ee] = be[ee * kPfStride + cc];  // (tensor-core score, position)
         }
         if (lane == 0) G.surv_cnt[gcol] = ovl ? -1 : cnt_c;
       }
     }
-    seq += n1 + ntiles;
+    seq += 2 * ntiles;
   }
 
-  // no copy into shared memory and no MMA may outlive the CTA
+  // no copy into shared memory and no MMA may outlive the CTA: the producer
+  // waits (bounded) for the last ring fills it issued
   if (warp == 0 && lane == 0) {
-    for (long long gs = seq - 1; gs >= 0 && gs >= seq - stages; --gs) {
+    for (long long gs = issued - 1; gs >= 0 && gs >= issued - stages; --gs) {
       if (!mbar_wait(&empty[gs % stages], (uint32_t)(gs / stages) & 1u))
         set_status(G.status, kStatusTimeout);
     }
@@ -569,6 +598,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 }
 
 // ------------------------------------------------------------ finalize -----
+
+// The float32 chain (acc = fma(q[c], k[c], acc), c = 0..D-1) of two bf16 key
+// rows against one query held as floats in shared memory; every load of both
+// rows is issued before the arithmetic, and the two chains are independent.
+template <int D>
+__device__ __forceinline__ void score_two_rows(const void* kbase, long long ra, long long rb,
+                                               const float* q, float& sa, float& sb) {
+  constexpr int NV = D / 8;  // 16-byte vectors per row
+  const uint4* pa = reinterpret_cast<const uint4*>(kbase) + ra * NV;
+  const uint4* pb = reinterpret_cast<const uint4*>(kbase) + rb * NV;
+  uint4 wa[NV], wb[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    wa[v] = __ldg(pa + v);
+    wb[v] = __ldg(pb + v);
+  }
+  const float4* q4 = reinterpret_cast<const float4*>(q);
+  float a = 0.f, b = 0.f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float4 qq = q4[v * 2 + h];
+      a = fmaf(qq.x, chunk_elem<true>(wa[v], 4 * h + 0), a);
+      b = fmaf(qq.x, chunk_elem<true>(wb[v], 4 * h + 0), b);
+      a = fmaf(qq.y, chunk_elem<true>(wa[v], 4 * h + 1), a);
+      b = fmaf(qq.y, chunk_elem<true>(wb[v], 4 * h + 1), b);
+      a = fmaf(qq.z, chunk_elem<true>(wa[v], 4 * h + 2), a);
+      b = fmaf(qq.z, chunk_elem<true>(wb[v], 4 * h + 2), b);
+      a = fmaf(qq.w, chunk_elem<true>(wa[v], 4 * h + 3), a);
+      b = fmaf(qq.w, chunk_elem<true>(wb[v], 4 * h + 3), b);
+    }
+  }
+  sa = a;
+  sb = b;
+}
 
 // One warp per column (= per output row): exact top-k from the survivors,
 // then the sorted top-k positions, C_i and the k-th key.  4 warps per block.
@@ -593,21 +658,84 @@ __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
   __syncwarp();
   const int cnt = G.surv_cnt[gcol];
   uint64_t x0;
-  if (cnt >= 0) {
-    // the survivors through the exact chain
+  if (cnt >= 0 && (cnt <= kk || G.thr)) {
+    // every survivor is selected, or the exact k-th key is needed (for the
+    // excluded mass): all survivors through the exact chain; a lane's two
+    // rows are loaded up front and their chains interleaved (independent)
     uint64_t x[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int ee = lane + 32 * r;
-      x[r] = 0ull;
-      if (ee < cnt) {
-        const uint32_t e = G.surv[gcol * kPfLL + ee];
-        const uint32_t j = e + 1u;
-        x[r] = rank_key(score_row_q4<true, D>(G.kp, kvrow0 + j, qs[warp]), j);
-      }
+    {
+      const float2 e0 = lane < cnt ? G.surv[gcol * kPfLL + lane] : make_float2(0.f, 0.f);
+      const float2 e1 = lane + 32 < cnt ? G.surv[gcol * kPfLL + lane + 32] : make_float2(0.f, 0.f);
+      const uint32_t j0 = (uint32_t)__float_as_int(e0.y), j1 = (uint32_t)__float_as_int(e1.y);
+      float s0, s1;
+      score_two_rows<D>(G.kp, kvrow0 + j0, kvrow0 + j1, qs[warp], s0, s1);
+      x[0] = lane < cnt ? rank_key(s0, j0) : 0ull;
+      x[1] = lane + 32 < cnt ? rank_key(s1, j1) : 0ull;
     }
     warp_sort_desc<2>(x, lane);
     x0 = x[0];
+  } else if (cnt >= 0) {
+    // More survivors than k.  A bisection on the tensor-core scores t finds V
+    // with fewer than k survivors at t >= V.  A survivor with t > V + 2 delta
+    // is in the exact top-k without rescoring: any key that beats it exactly
+    // has t > V (|t - exact| <= delta), every key with t > V is a survivor,
+    // and fewer than k of them exist.  Only the other survivors (near the
+    // boundary, typically a handful) are rescored with the exact chain, and
+    // the best of them fill the remaining slots.
+    const float2 e0 = lane < cnt ? G.surv[gcol * kPfLL + lane] : make_float2(-INFINITY, 0.f);
+    const float2 e1 = lane + 32 < cnt ? G.surv[gcol * kPfLL + lane + 32]
+                                      : make_float2(-INFINITY, 0.f);
+    float lo = warp_max(-fminf(e0.x == -INFINITY ? INFINITY : e0.x,
+                               e1.x == -INFINITY ? INFINITY : e1.x));
+    lo = -lo;  // smallest t: kk <= cnt survivors are >= it
+    float hi = warp_max(fmaxf(e0.x, e1.x));
+    hi = hi + fabsf(hi) * 1e-6f + 1e-30f;  // no survivor is >= it
+#pragma unroll 1
+    for (int it = 0; it < 16; ++it) {
+      const float mid = 0.5f * (lo + hi);
+      const int c = __popc(__ballot_sync(kFull, e0.x >= mid)) +
+                    __popc(__ballot_sync(kFull, e1.x >= mid));
+      if (c >= kk) lo = mid;
+      else hi = mid;
+    }
+    float qn1 = 0.f;
+    for (int c = lane; c < D; c += 32) qn1 += fabsf(qs[warp][c]);  // the bf16 inputs, exactly
+    qn1 = warp_sum(qn1);
+    const float two_delta =
+        2.f * tc_delta_factor(D) * qn1 * 1.01f * __uint_as_float(G.kmax[bh]);
+    const float V = hi + two_delta;
+    const bool c0 = e0.x > V, c1 = e1.x > V;                  // certain
+    const bool u0 = lane < cnt && !c0, u1 = lane + 32 < cnt && !c1;  // to rescore
+    const unsigned bc0 = __ballot_sync(kFull, c0), bc1 = __ballot_sync(kFull, c1);
+    const unsigned bu0 = __ballot_sync(kFull, u0), bu1 = __ballot_sync(kFull, u1);
+    const int m = __popc(bc0) + __popc(bc1);  // < kk
+    const int u = __popc(bu0) + __popc(bu1);  // >= kk - m
+    const unsigned below = (1u << lane) - 1u;
+    uint64_t* sb = scratch[warp];
+    if (c0) sb[__popc(bc0 & below)] = rank_key(0.f, (uint32_t)__float_as_int(e0.y));
+    if (c1) sb[__popc(bc0) + __popc(bc1 & below)] = rank_key(0.f, (uint32_t)__float_as_int(e1.y));
+    if (u0) sb[64 + __popc(bu0 & below)] = (uint64_t)(uint32_t)__float_as_int(e0.y);
+    if (u1) sb[64 + __popc(bu0) + __popc(bu1 & below)] = (uint64_t)(uint32_t)__float_as_int(e1.y);
+    __syncwarp();
+    uint64_t x[2] = {0ull, 0ull};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      if (i < u) {
+        const uint32_t j = (uint32_t)sb[64 + i];
+        x[r] = rank_key(score_row_q4<true, D>(G.kp, kvrow0 + j, qs[warp]), j);
+      }
+    }
+    if (u > 32) {
+      warp_sort_desc<2>(x, lane);
+    } else {
+      uint64_t y1[1] = {x[0]};
+      warp_sort_desc<1>(y1, lane);
+      x[0] = y1[0];
+    }
+    const uint64_t unc = __shfl_sync(kFull, x[0], (lane - m) & 31);
+    const uint64_t cer = sb[lane < m ? lane : 0];
+    x0 = lane < m ? cer : unc;  // lanes < k: the selected set (not in exact order)
   } else {
     // the near ties overflowed: every candidate through the exact chain
     uint64_t fthr = 0ull;
