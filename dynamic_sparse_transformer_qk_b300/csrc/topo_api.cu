@@ -37,6 +37,7 @@ struct Plan {
   // workspace layout (bytes)
   size_t off_cnt = 0, off_cnt_e = 0, off_kmax = 0, off_work = 0, off_zero_end = 0;
   size_t off_lists = 0, off_thr = 0, off_part = 0, off_surv = 0, off_scnt = 0, off_topk = 0;
+  size_t off_topl = 0;
   size_t total = 0;
 };
 
@@ -244,6 +245,8 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
       o = align256(o + ncolumns * 4);
       P->off_topk = o;
       o = align256(o + ncolumns * p->k * 4);
+      P->off_topl = o;
+      o = align256(o + ncolumns * p->k * 4);
     }
   } else {
     P->off_part = o;
@@ -379,6 +382,7 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
     G.surv = reinterpret_cast<float2*>(w + P.off_surv);
     G.surv_cnt = reinterpret_cast<int*>(w + P.off_scnt);
     G.topsel = reinterpret_cast<int*>(w + P.off_topk);
+    G.toplogit = out ? reinterpret_cast<float*>(w + P.off_topl) : nullptr;  // softmax logits
     G.nitems = P.pf_nitems;
     G.items_per_head = P.pf_items_per_head;
     G.thr_nc = P.NC;

@@ -61,6 +61,7 @@ struct Geom {
   int* surv_cnt;              // [column] survivors, -1 when the buffer overflowed
   int* work;                  // work-queue counter of the scan kernel
   int* topsel;                // [row][k] selected positions ascending, -1 padded
+  float* toplogit;            // [row][k] logits (scale * score) of topsel's positions
   long long nitems;           // scan work items (blocks of 128 columns)
   int items_per_head;         // blocks per (sequence, KV head)
   int thr_nc;                 // columns per unit of the excluded-mass pass

@@ -172,6 +172,16 @@ cudaError_t Launcher<BF16, D>::prefill(const CUtensorMap& mk128, const Geom& G, 
     prefill_finalize_kernel<D><<<(unsigned)((ncolumns + 3) / 4), 128, 0, st>>>(G);
     e = cudaGetLastError();
     if (e != cudaSuccess || !do_pv) return e;
+    const int pb_smem = PbSmem(D, G.W).total;
+    if (pb_smem <= kMaxSmem) {
+      // the window band of a block of rows fits in shared memory
+      constexpr auto band = &prefill_pv_band_kernel<D>;
+      e = allow_smem<band>();
+      if (e != cudaSuccess) return e;
+      const dim3 gb((unsigned)((G.nq + kPbRows - 1) / kPbRows), (unsigned)G.Hkv, (unsigned)G.B);
+      band<<<gb, kPbWarps * 32, pb_smem, st>>>(G);
+      return cudaGetLastError();
+    }
     prefill_pv_kernel<D><<<(unsigned)((ncolumns + 3) / 4), 128, 0, st>>>(G);
     return cudaGetLastError();
   }

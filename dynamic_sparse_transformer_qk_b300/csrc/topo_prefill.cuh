@@ -712,8 +712,8 @@ __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
     const int u = __popc(bu0) + __popc(bu1);  // >= kk - m
     const unsigned below = (1u << lane) - 1u;
     uint64_t* sb = scratch[warp];
-    if (c0) sb[__popc(bc0 & below)] = rank_key(0.f, (uint32_t)__float_as_int(e0.y));
-    if (c1) sb[__popc(bc0) + __popc(bc1 & below)] = rank_key(0.f, (uint32_t)__float_as_int(e1.y));
+    if (c0) sb[__popc(bc0 & below)] = rank_key(e0.x, (uint32_t)__float_as_int(e0.y));
+    if (c1) sb[__popc(bc0) + __popc(bc1 & below)] = rank_key(e1.x, (uint32_t)__float_as_int(e1.y));
     if (u0) sb[64 + __popc(bu0 & below)] = (uint64_t)(uint32_t)__float_as_int(e0.y);
     if (u1) sb[64 + __popc(bu0) + __popc(bu1 & below)] = (uint64_t)(uint32_t)__float_as_int(e1.y);
     __syncwarp();
@@ -734,7 +734,13 @@ __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
       x[0] = y1[0];
     }
     const uint64_t unc = __shfl_sync(kFull, x[0], (lane - m) & 31);
-    const uint64_t cer = sb[lane < m ? lane : 0];
+    uint64_t cer = lane < m ? sb[lane] : 0ull;
+    if (lane < m && G.toplogit) {
+      // a certain key's exact score (its logit in the softmax; the selection
+      // did not need it)
+      const uint32_t j = key_pos(sb[lane]);
+      cer = rank_key(score_row_q4<true, D>(G.kp, kvrow0 + j, qs[warp]), j);
+    }
     x0 = lane < m ? cer : unc;  // lanes < k: the selected set (not in exact order)
   } else {
     // the near ties overflowed: every candidate through the exact chain
@@ -770,15 +776,20 @@ __global__ void __launch_bounds__(128) prefill_finalize_kernel(const Geom G) {
       G.thr[(size_t)unit * G.thr_nc + slot] = kk == 0 ? ~0ull : (t < kk ? 0ull : kth);
     }
   }
-  // selected positions ascending
-  uint64_t y = mine ? (~0ull - (uint64_t)key_pos(mine)) : 0ull;
+  // selected positions ascending, each with its exact score
+  uint64_t y = mine ? (((uint64_t)(0xffffffffu - key_pos(mine)) << 32) |
+                       __float_as_uint(key_score(mine)))
+                    : 0ull;
   {
     uint64_t ya[1] = {y};
     warp_sort_desc<1>(ya, lane);
     y = ya[0];
   }
-  const int tj = y ? (int)(~0ull - y) : -1;
-  if (lane < kk) G.topsel[row * kk + lane] = tj;
+  const int tj = y ? (int)(0xffffffffu - (uint32_t)(y >> 32)) : -1;
+  if (lane < kk) {
+    G.topsel[row * kk + lane] = tj;
+    if (G.toplogit) G.toplogit[row * kk + lane] = y ? G.scale * __uint_as_float((uint32_t)y) : 0.f;
+  }
   if (G.idx) {
     const long long cmax = 1 + (long long)G.W + kk;
     const bool wide = p - G.W + 1 <= 0;
@@ -840,6 +851,273 @@ __global__ void __launch_bounds__(128) prefill_pv_kernel(const Geom G) {
   warp_softmax_pv_with<true, D>(
       G, kvrow0, [&](long long kr) { return score_row_q4<true, D>(G.kp, kr, qw); }, mEnt, entry,
       wsm[warp], jsm[warp], G.out + row * D, lane);
+}
+
+// ------------------------------------------------------- banded softmax ----
+//
+// The softmax over C_i and the weighted sum of V for a block of kPbRows
+// consecutive rows of every query head of one KV head.  Their windows all lie
+// in the band [p0 - W + 1, p0 + kPbRows - 1] (p0: the block's first
+// position), whose K and V rows are staged in shared memory once and shared
+// by the block's g * kPbRows (row, head) pairs.  A warp takes four rows of one
+// head at a time, so every staged row it reads serves four rows.  The anchor's
+// rows are staged too.  The top-k entries' logits come from the finalize step
+// (scale times the exact float32 score); only their V rows are gathered from
+// global memory.  Logits of window keys are float32 dot products of the
+// bf16 inputs; the softmax and the sums are float32.
+constexpr int kPbRows = 32;   // rows per block (per query head)
+constexpr int kPbWarps = 8;
+constexpr int kPbUnit = 4;    // rows per warp step
+
+// Shared-memory carve-up of the banded kernel (host and device).  Staged rows
+// are padded by 16 bytes so that consecutive rows start four banks apart.
+struct PbSmem {
+  int kb, vb, k0, v0, q, lw, bars, total;
+  __host__ __device__ PbSmem(int D, int W) {
+    const int rowb = D * 2 + 16;
+    const int nb = W + kPbRows - 1;
+    const int wb = W + kPbUnit - 1;
+    int o = 0;
+    kb = o; o += nb * rowb;
+    vb = o; o += nb * rowb;
+    k0 = o; o += rowb;
+    v0 = o; o += rowb;
+    q = o;  o += kPbWarps * kPbUnit * D * 4;                 // float q rows per warp
+    lw = o; o += kPbWarps * kPbUnit * ((wb + 3) & ~3) * 4;   // window logits / weights
+    bars = o; o += 16;
+    total = o + 16;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPbWarps * 32, 1) prefill_pv_band_kernel(const Geom G) {
+  using S = Shape<true, D>;
+  constexpr int ROWP = S::ROWB + 16;  // staged row pitch
+  constexpr int EPL = D / 32;         // output elements per lane
+  extern __shared__ __align__(16) uint8_t pb_raw[];
+  uint8_t* sm = pb_raw + ((16u - (smem_addr(pb_raw) & 15u)) & 15u);
+  const PbSmem L(D, G.W);
+  uint8_t* kb = sm + L.kb;
+  uint8_t* vb = sm + L.vb;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bars);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kk = G.topk;
+  const int W = G.W;
+  const int wb = W + kPbUnit - 1;
+  const int wbp = (wb + 3) & ~3;
+  float* qw = reinterpret_cast<float*>(sm + L.q) + warp * kPbUnit * D;
+  float* lw = reinterpret_cast<float*>(sm + L.lw) + warp * kPbUnit * wbp;
+
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const long long r0 = (long long)blockIdx.x * kPbRows;  // first row of the block
+  const long long rend = r0 + kPbRows < G.nq ? r0 + kPbRows : G.nq;
+  const long long p0 = G.n - G.nq + r0;
+  const long long band_lo = p0 - W + 1 > 0 ? p0 - W + 1 : 0;
+  const long long band_hi = G.n - G.nq + rend - 1;
+  const int nb = (int)(band_hi - band_lo + 1);
+  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
+  const uint8_t* kg = reinterpret_cast<const uint8_t*>(G.kp);
+  const uint8_t* vg = reinterpret_cast<const uint8_t*>(G.vp);
+
+  // stage the band and the anchor (bulk copies completing on one barrier)
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) mbar_arrive_expect_tx(bar, (uint32_t)((nb + 1) * 2 * S::ROWB));
+  for (int i = tid; i <= nb; i += blockDim.x) {
+    const long long row = i < nb ? band_lo + i : 0;
+    uint8_t* dk = i < nb ? kb + (size_t)i * ROWP : sm + L.k0;
+    uint8_t* dv = i < nb ? vb + (size_t)i * ROWP : sm + L.v0;
+    bulk_copy_g2s(dk, kg + (kvrow0 + row) * S::ROWB, S::ROWB, bar);
+    bulk_copy_g2s(dv, vg + (kvrow0 + row) * S::ROWB, S::ROWB, bar);
+  }
+  const bool staged = mbar_wait(bar, 0);
+  if (!staged && tid == 0) set_status(G.status, kStatusTimeout);
+  if (__syncthreads_or(!staged)) return;
+
+  const int units = G.g * kPbRows / kPbUnit;
+  for (int u = warp; u < units; u += kPbWarps) {
+    const int hh = u / (kPbRows / kPbUnit);
+    const long long ru = r0 + (long long)(u % (kPbRows / kPbUnit)) * kPbUnit;  // first row
+    if (ru >= rend) continue;
+    const int nr = (int)(rend - ru < kPbUnit ? rend - ru : kPbUnit);
+    const int h = kvh * G.g + hh;
+    const long long rowbase = ((long long)b * G.Hq + h) * G.nq;
+    const long long pu = G.n - G.nq + ru;  // position of the unit's first row
+    __syncwarp();
+    for (int i = lane; i < kPbUnit * D; i += 32) {
+      const int r = i / D, c = i % D;
+      qw[i] = r < nr ? load_elem<true>(G.qp, (rowbase + ru + r) * D + c) : 0.f;
+    }
+    // top-k entries of the unit's rows (lane i: entry i of each row)
+    int tp[kPbUnit];
+    float tl[kPbUnit];
+#pragma unroll
+    for (int r = 0; r < kPbUnit; ++r) {
+      tp[r] = -1;
+      tl[r] = -INFINITY;
+      if (r < nr && lane < kk) {
+        const long long row = rowbase + ru + r;
+        tp[r] = G.topsel[row * kk + lane];
+        if (tp[r] >= 0) tl[r] = G.toplogit[row * kk + lane];
+      }
+    }
+    __syncwarp();
+    // window logits: the union of the rows' windows [jlo, pu + nr - 1]
+    const long long jlo = pu - W + 1 > 0 ? pu - W + 1 : 0;
+    const int nw = (int)(pu + nr - 1 - jlo + 1);
+    float mx[kPbUnit];
+#pragma unroll
+    for (int r = 0; r < kPbUnit; ++r) mx[r] = -INFINITY;
+    // two keys per lane at a time (e and e + 32): eight independent chains,
+    // every query load serves both
+    for (int e0 = 0; e0 < nw; e0 += 64) {
+      const int ea = e0 + lane, eb = e0 + 32 + lane;
+      const bool va = ea < nw, vbk = eb < nw;
+      const uint4* kra = reinterpret_cast<const uint4*>(kb + (size_t)(jlo + (va ? ea : 0) - band_lo) * ROWP);
+      const uint4* krb = reinterpret_cast<const uint4*>(kb + (size_t)(jlo + (vbk ? eb : 0) - band_lo) * ROWP);
+      float aa[kPbUnit], ab[kPbUnit];
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) {
+        aa[r] = 0.f;
+        ab[r] = 0.f;
+      }
+#pragma unroll 2
+      for (int v = 0; v < S::ROWB / 16; ++v) {
+        const uint4 wa4 = kra[v], wb4 = krb[v];
+        float xa[8], xb[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          xa[x] = chunk_elem<true>(wa4, x);
+          xb[x] = chunk_elem<true>(wb4, x);
+        }
+#pragma unroll
+        for (int r = 0; r < kPbUnit; ++r) {
+          const float4* q4 = reinterpret_cast<const float4*>(qw + r * D + v * 8);
+          const float4 qa = q4[0], qb = q4[1];
+          const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            aa[r] = fmaf(qq[x], xa[x], aa[r]);
+            ab[r] = fmaf(qq[x], xb[x], ab[r]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) {
+        const long long p = pu + r;
+        const long long ja = jlo + ea, jb = jlo + eb;
+        const bool ina = va && r < nr && ja <= p && ja >= p - W + 1;
+        const bool inb = vbk && r < nr && jb <= p && jb >= p - W + 1;
+        const float la = ina ? G.scale * aa[r] : -INFINITY;
+        const float lb = inb ? G.scale * ab[r] : -INFINITY;
+        if (va) lw[r * wbp + ea] = la;
+        if (vbk) lw[r * wbp + eb] = lb;
+        mx[r] = fmaxf(mx[r], fmaxf(la, lb));
+      }
+    }
+    // anchor logit of rows whose window does not reach position 0
+    float la[kPbUnit];
+    {
+      float pa[kPbUnit];
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) pa[r] = 0.f;
+      const uint32_t* k0w = reinterpret_cast<const uint32_t*>(sm + L.k0);
+      for (int c2 = lane; c2 < D / 2; c2 += 32) {
+        const uint32_t wv = k0w[c2];
+        const float ka = __uint_as_float(wv << 16), kb2 = __uint_as_float(wv & 0xffff0000u);
+#pragma unroll
+        for (int r = 0; r < kPbUnit; ++r)
+          pa[r] = fmaf(qw[r * D + 2 * c2 + 1], kb2, fmaf(qw[r * D + 2 * c2], ka, pa[r]));
+      }
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) {
+        const float sa = warp_sum(pa[r]);
+        const bool sep = r < nr && pu + r - W + 1 > 0;  // anchor outside the window
+        la[r] = sep ? G.scale * sa : -INFINITY;
+        mx[r] = fmaxf(fmaxf(mx[r], la[r]), tl[r]);
+      }
+    }
+    float z[kPbUnit], tw[kPbUnit], wa[kPbUnit];
+#pragma unroll
+    for (int r = 0; r < kPbUnit; ++r) {
+      mx[r] = warp_max(mx[r]);
+      tw[r] = tl[r] == -INFINITY ? 0.f : expf(tl[r] - mx[r]);
+      wa[r] = la[r] == -INFINITY ? 0.f : expf(la[r] - mx[r]);
+      z[r] = tw[r] + (lane == 0 ? wa[r] : 0.f);
+    }
+    __syncwarp();
+    for (int e = lane; e < nw; e += 32) {
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) {
+        const float l = lw[r * wbp + e];
+        const float w = l == -INFINITY ? 0.f : expf(l - mx[r]);
+        lw[r * wbp + e] = w;
+        z[r] += w;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kPbUnit; ++r) z[r] = warp_sum(z[r]);
+    __syncwarp();
+    // weighted sums: lane owns output elements lane*EPL ..
+    float acc[kPbUnit][EPL];
+    {
+      float va[EPL];
+      lane_elems<true, D>(sm + L.v0 + lane * S::BPL, va);
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) {
+        const float w0 = __shfl_sync(kFull, wa[r], 0);
+#pragma unroll
+        for (int x = 0; x < EPL; ++x) acc[r][x] = w0 * va[x];
+      }
+    }
+#pragma unroll 2
+    for (int e = 0; e < nw; ++e) {
+      float vv[EPL];
+      lane_elems<true, D>(vb + (size_t)(jlo + e - band_lo) * ROWP + lane * S::BPL, vv);
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) {
+        const float w = lw[r * wbp + e];
+#pragma unroll
+        for (int x = 0; x < EPL; ++x) acc[r][x] = fmaf(w, vv[x], acc[r][x]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kPbUnit; ++r) {
+      const int t = __popc(__ballot_sync(kFull, tp[r] >= 0));
+      // the gathered V rows, eight loads in flight per lane
+      int i = 0;
+      for (; i + 8 <= t; i += 8) {
+        float vv[8][EPL];
+        float ww[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int j = __shfl_sync(kFull, tp[r], i + q);
+          ww[q] = __shfl_sync(kFull, tw[r], i + q);
+          lane_elems<true, D>(vg + (kvrow0 + j) * S::ROWB + lane * S::BPL, vv[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int x = 0; x < EPL; ++x) acc[r][x] = fmaf(ww[q], vv[q][x], acc[r][x]);
+      }
+      for (; i < t; ++i) {
+        const int j = __shfl_sync(kFull, tp[r], i);
+        const float w = __shfl_sync(kFull, tw[r], i);
+        float vv[EPL];
+        lane_elems<true, D>(vg + (kvrow0 + j) * S::ROWB + lane * S::BPL, vv);
+#pragma unroll
+        for (int x = 0; x < EPL; ++x) acc[r][x] = fmaf(w, vv[x], acc[r][x]);
+      }
+      if (r < nr) {
+        float* o = G.out + (rowbase + ru + r) * D + lane * EPL;
+#pragma unroll
+        for (int x = 0; x < EPL; ++x) o[x] = z[r] > 0.f ? acc[r][x] / z[r] : 0.f;
+      }
+    }
+  }
 }
 
 }  // namespace topo
