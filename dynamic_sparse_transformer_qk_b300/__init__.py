@@ -150,8 +150,19 @@ def _stream(stream, device=None) -> int:
     return s.cuda_stream
 
 
+_ws_sizes: dict = {}
+
+
+def _params_key(p: Params) -> tuple:
+    return (p.B, p.Hq, p.Hkv, p.d, p.n, p.nq, p.kv_stride, p.W, p.k, p.scale, p.dtype)
+
+
 def workspace_size(p: Params) -> int:
-    return int(load_library().topo_attn_workspace_size(ctypes.byref(p)))
+    key = _params_key(p)
+    need = _ws_sizes.get(key)
+    if need is None:
+        need = _ws_sizes[key] = int(load_library().topo_attn_workspace_size(ctypes.byref(p)))
+    return need
 
 
 def dense_workspace_size(p: Params) -> int:

@@ -1,14 +1,17 @@
 // topo_api.cu -- the C ABI of libtopoattn.so (declared in include/topo_attn.h):
 // argument checks, launch planning, workspace layout, TMA descriptors and
 // kernel dispatch.  No allocation, no synchronisation (except the explicit
-// status read-back), no global mutable state beyond lazily resolved driver
-// entry points and per-kernel attribute set-up.  Each call clears the split
-// counters it uses (one cudaMemsetAsync on the caller's stream), so a
-// workspace may be shared by calls of any shapes, in stream order.
+// status read-back).  Global state: lazily resolved driver entry points,
+// per-kernel attribute set-up and a small mutex-guarded cache of launch plans
+// (a plan depends only on the parameters and the device).  Each call clears
+// the split counters it uses (one cudaMemsetAsync on the caller's stream), so
+// a workspace may be shared by calls of any shapes, in stream order.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "topo_attn.h"
 #include "topo_launch.cuh"
@@ -256,6 +259,54 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
   return TOPO_OK;
 }
 
+// make_plan, memoised: the last kPlanCache distinct (parameters, pass, device)
+// triples (the split search costs tens of microseconds for long caches).
+constexpr int kPlanCache = 32;
+struct PlanEntry {
+  topo_attn_params p;
+  int dense, dev, rc, valid;
+  Plan plan;
+};
+std::mutex g_plan_mu;
+PlanEntry g_plans[kPlanCache];
+int g_plan_next = 0;
+
+bool same_params(const topo_attn_params& a, const topo_attn_params& b) {
+  return a.B == b.B && a.Hq == b.Hq && a.Hkv == b.Hkv && a.d == b.d && a.n == b.n &&
+         a.nq == b.nq && a.kv_stride == b.kv_stride && a.W == b.W && a.k == b.k &&
+         memcmp(&a.scale, &b.scale, sizeof a.scale) == 0 && a.dtype == b.dtype;
+}
+
+int make_plan_cached(const topo_attn_params* p, bool dense, Plan* P) {
+  if (!p) return TOPO_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (int i = 0; i < kPlanCache; ++i) {
+      const PlanEntry& e = g_plans[i];
+      if (e.valid && e.dense == (int)dense && e.dev == dev && same_params(e.p, *p)) {
+        *P = e.plan;
+        return e.rc;
+      }
+    }
+  }
+  const int rc = make_plan(p, dense, P);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  PlanEntry& e = g_plans[g_plan_next];
+  g_plan_next = (g_plan_next + 1) % kPlanCache;
+  e.p = *p;
+  e.dense = (int)dense;
+  e.dev = dev;
+  e.rc = rc;
+  e.plan = *P;
+  e.valid = 1;
+  return rc;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
@@ -340,7 +391,7 @@ int dispatch(bool bf16, int D, F&& f) {
 int run_topo(const topo_attn_params* p, const void* q, const void* k, const void* v, float* out,
              int32_t* idx, float* excl, void* ws, size_t ws_bytes, cudaStream_t st) {
   Plan P;
-  int rc = make_plan(p, false, &P);
+  int rc = make_plan_cached(p, false, &P);
   if (rc != TOPO_OK) return rc;
   if (!q || !k) return TOPO_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || (v && !aligned16(v))) return TOPO_ERR_INVALID_ARG;
@@ -420,12 +471,12 @@ extern "C" {
 
 size_t topo_attn_workspace_size(const topo_attn_params* p) {
   Plan P;
-  return make_plan(p, false, &P) == TOPO_OK ? P.total : 0;
+  return make_plan_cached(p, false, &P) == TOPO_OK ? P.total : 0;
 }
 
 size_t dense_attn_workspace_size(const topo_attn_params* p) {
   Plan P;
-  return make_plan(p, true, &P) == TOPO_OK ? P.total : 0;
+  return make_plan_cached(p, true, &P) == TOPO_OK ? P.total : 0;
 }
 
 int topo_attn_workspace_init(void* ws, size_t bytes, topo_stream_t stream) {
@@ -472,7 +523,7 @@ int topo_attn_sparse_softmax_pv(const topo_attn_params* p, const void* q, const 
 int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, const void* v,
                        float* out, void* ws, size_t ws_bytes, topo_stream_t stream) {
   Plan P;
-  int rc = make_plan(p, true, &P);
+  int rc = make_plan_cached(p, true, &P);
   if (rc != TOPO_OK) return rc;
   if (!q || !k || !v || !out) return TOPO_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return TOPO_ERR_INVALID_ARG;
@@ -525,7 +576,7 @@ size_t topo_attn_layers_workspace_size(const topo_attn_params* p, const topo_lay
   for (int l = 0; l < L; ++l) {
     const topo_attn_params lp = layer_params(p, layers[l]);
     Plan P;
-    if (make_plan(&lp, layers[l].dense != 0, &P) != TOPO_OK) return 0;
+    if (make_plan_cached(&lp, layers[l].dense != 0, &P) != TOPO_OK) return 0;
     need = P.total > need ? P.total : need;
   }
   return need;
@@ -539,7 +590,7 @@ int topo_attn_layers_forward(const topo_attn_params* p, const topo_layer* layers
     const topo_layer& ly = layers[l];
     const topo_attn_params lp = layer_params(p, ly);
     Plan P;
-    const int rc = make_plan(&lp, ly.dense != 0, &P);
+    const int rc = make_plan_cached(&lp, ly.dense != 0, &P);
     if (rc != TOPO_OK) return rc;
     if (ly.reserved != 0 || !ly.q || !ly.k || !ly.v || !ly.out) return TOPO_ERR_INVALID_ARG;
     if (!aligned16(ly.q) || !aligned16(ly.k) || !aligned16(ly.v)) return TOPO_ERR_INVALID_ARG;

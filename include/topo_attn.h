@@ -30,8 +30,9 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
- *     library allocates nothing and keeps no global mutable state (the one
- *     exception is topo_attn_forward_noalloc's fixed scratch array); it is
+ *     library allocates nothing.  Its only global mutable state is a small
+ *     mutex-guarded cache of launch plans (keyed by the parameters and the
+ *     device) and topo_attn_forward_noalloc's fixed scratch array; it is
  *     thread-safe.  Work is enqueued on `stream` (a cudaStream_t, 0 = legacy
  *     default stream) and the call returns without synchronising.
  *   - Layouts are row-major with d fastest:
