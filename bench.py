@@ -425,6 +425,91 @@ def measure_decode(args, w: synth.Workload, dev, rank: int, world: int, local: i
     return rec
 
 
+def measure_layers(args, dev, local: int, *, steps: int, L: int = 32, n: int = 131072,
+                   cpu_budget: float = 0.0) -> dict:
+    """One decode step through L layers (topo_attn_layers_forward): layer l
+    has its own q and its own K/V cache of n tokens (32/8 heads, d=128,
+    bf16); pillar layers (every 16th, from layer 0) attend densely, the
+    others use windows 256 / 128 / 64 by depth third and k = 32.  Timed as
+    CUDA graph replays; beside it, the same step with every layer dense."""
+    import torch
+    import dynamic_sparse_transformer_qk_b300 as topo
+
+    base = synth.CONFIGS[1].with_(n=n, name=f"decode n={n} bf16 32/8 heads, {L} layers")
+    sch = topo.layer_schedule(L, pillar_every=16, windows=(256, 128, 64), topk=32)
+    qs, ks, vs = [], [], []
+    x0 = None
+    for l in range(L):
+        x = synth.make(base.with_(seed=base.seed + 101 * (l + 1)))
+        if l == 1:
+            x0 = x  # a sparse layer's inputs, for the CPU baseline
+        qs.append(torch.from_numpy(x["q"]).view(torch.bfloat16).to(dev))
+        ks.append(torch.from_numpy(x["k"]).view(torch.bfloat16).to(dev))
+        vs.append(torch.from_numpy(x["v"]).view(torch.bfloat16).to(dev))
+    outs = [torch.empty((1, base.Hq, 1, base.d), dtype=torch.float32, device=dev)
+            for _ in range(L)]
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(schedule):
+        ws = topo.Workspace(dev)
+
+        def step():
+            topo.layers_forward(qs, ks, vs, schedule, n=n, scale=base.scale, outs=outs,
+                                workspace=ws)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    with ClockSampler(local) as clk:
+        time.sleep(0.2)
+        ms = timed(sch)
+        dense_sch = [dict(s, dense=True) for s in sch]
+        dense_ms = timed(dense_sch)
+    es = 2
+    k_bytes = base.Hkv * n * base.d * es
+    io = base.Hq * base.d * (es + 4)
+    alg = sum(2 * k_bytes + io if s["dense"] else decode_alg_bytes(base.with_(W=s["W"], k=s["topk"]))
+              for s in sch)
+    peaks = load_peaks()
+    achieved = alg / (ms / 1000.0) / 1e9
+    rec = {"ms_per_step": ms, "value": 1000.0 / ms, "unit": "queries/s",
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                        "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                        "algorithmic_bytes_per_step": alg,
+                        "kernel": "topo_select_tc_kernel (sparse layers) + dense_kernel (pillars)",
+                        "timing": f"CUDA events around each replay of the captured {L}-layer step",
+                        "traffic": None},
+           "all_dense_ms_per_step": dense_ms, "pillar_speedup_vs_all_dense": dense_ms / ms,
+           "clocks": clk.summary(), "gpu_launches": 2 * L * steps,
+           "config": {"workload": f"{L} layers x (decode n={n}, 32/8 heads, d=128, bf16); "
+                                  "pillars (dense) at layers 0 and 16; W 256/128/64 by depth "
+                                  "third; k=32; every layer its own seeded q, K, V",
+                      "schedule": [("dense" if s["dense"] else f"W{s['W']}") for s in sch],
+                      "l2": f"{2 * k_bytes * L / 1e9:.1f} GB of K/V >> 126 MB L2; no flush"}}
+    if cpu_budget > 0:
+        # the oracle on one sparse layer's rows, scaled to the whole step (the
+        # dense layers cost about as much per row as the sparse ones there)
+        r = oracle_rate(base.with_(W=sch[1]["W"]), x0, budget_s=cpu_budget)
+        rec["cpu_baseline"] = dict(r, value=r["value"] / L,
+                                   sample=r["sample"] + f"; scaled to {L} layers per query")
+    del qs, ks, vs
+    return rec
+
+
 def bench_ours(args, w: synth.Workload):
     import torch
     import torch.distributed as dist
@@ -456,6 +541,10 @@ def bench_ours(args, w: synth.Workload):
                            e2e=True, dense=True,
                            cpu_budget=0.0 if args.no_cpu_baseline else 5.0)
         subs.append(dict(name="decode-32k", metric=METRIC, **r))
+        torch.cuda.empty_cache()
+        r = measure_layers(args, dev, local, steps=sub_steps,
+                           cpu_budget=0.0 if args.no_cpu_baseline else 5.0)
+        subs.append(dict(name="decode-32-layers-128k", metric=METRIC, **r))
         torch.cuda.empty_cache()
         px = synth.make(synth.CONFIGS[3])
         for W in synth.PREFILL_WINDOWS:

@@ -59,6 +59,9 @@ def _load():
             lib.orc_topo_attn.restype = ctypes.c_int
             lib.orc_topo_attn.argtypes = [ctypes.POINTER(Params)] + [ctypes.c_void_p] * 4 + [
                 ctypes.c_int64] + [ctypes.c_void_p] * 6 + [ctypes.c_int]
+            lib.orc_topo_attn_group.restype = ctypes.c_int
+            lib.orc_topo_attn_group.argtypes = [ctypes.POINTER(Params)] + [ctypes.c_void_p] * 4 + [
+                ctypes.c_int64] + [ctypes.c_void_p] * 2 + [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -120,6 +123,43 @@ def topo_attn(P: Params, q: np.ndarray, k: np.ndarray, v: np.ndarray, rows=None,
     rc = lib.orc_topo_attn(ctypes.byref(P), q.ctypes.data, k.ctypes.data, v.ctypes.data,
                            None if rows_arr is None else rows_arr.ctypes.data, nrows,
                            *ptrs, int(nthreads or threads()))
+    if rc != 0:
+        raise ValueError("oracle rejected the parameters")
+    return res
+
+
+def topo_attn_group(P: Params, q: np.ndarray, k: np.ndarray, v: np.ndarray, rows=None,
+                    want=("out", "idx"), nthreads=None) -> dict:
+    """Group-shared selection (one condensate set per sequence, KV head and
+    row, shared by the KV head's g query heads; the top-k ranks keys by the
+    largest of the heads' float32 scores).  rows: flat ids over [B, Hkv, nq]
+    (None = all).  Returns ``out`` float64 [nrows, g, d] and ``idx`` int32
+    [nrows, 1+W+k]."""
+    lib = _load()
+    edt = np.float32 if P.dtype == 0 else np.uint16
+    for name, a, shape in (("q", q, (P.B, P.Hq, P.nq, P.d)),
+                           ("k", k, (P.B, P.Hkv, P.kv_stride, P.d)),
+                           ("v", v, (P.B, P.Hkv, P.kv_stride, P.d))):
+        if a.dtype != edt or tuple(a.shape) != shape or not a.flags.c_contiguous:
+            raise ValueError(f"{name}: expected contiguous {edt.__name__}{shape}")
+    g = P.Hq // P.Hkv
+    if rows is None:
+        nrows, rows_arr = P.B * P.Hkv * P.nq, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = rows_arr.size
+        if nrows and (rows_arr.min() < 0 or rows_arr.max() >= P.B * P.Hkv * P.nq):
+            raise ValueError("row id out of range")
+    res = {}
+    if "out" in want:
+        res["out"] = np.empty((nrows, g, P.d), dtype=np.float64)
+    if "idx" in want:
+        res["idx"] = np.empty((nrows, 1 + P.W + P.k), dtype=np.int32)
+    rc = lib.orc_topo_attn_group(ctypes.byref(P), q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                 None if rows_arr is None else rows_arr.ctypes.data, nrows,
+                                 res["out"].ctypes.data if "out" in res else None,
+                                 res["idx"].ctypes.data if "idx" in res else None,
+                                 int(nthreads or threads()))
     if rc != 0:
         raise ValueError("oracle rejected the parameters")
     return res

@@ -285,3 +285,162 @@ int orc_topo_attn(const orc_params *P, const void *q, const void *k, const void 
   pthread_mutex_destroy(&J.mu);
   return 0;
 }
+
+/* ---- group-shared selection (GQA) ---------------------------------------- */
+/*
+ * A variant the pages allow for grouped-query attention models (the method is
+ * validated on GQA architectures, Technical Summary section 4): one
+ * condensate set per (sequence, KV head, query row), shared by the g query
+ * heads that read that KV head.  Reading fixed here (the pages give no rule):
+ * the top-k ranks candidate j by the group score
+ *     shat_j = max over the group's heads h of s_{h,j}
+ * (s: the float32 ranking score of step 1), larger first, ties to the smaller
+ * index.  Anchor and window are as for one head.  Each head then takes its
+ * own float64 softmax over the shared set, with its own logits.
+ */
+typedef struct {
+  const orc_params *P;
+  const void *q, *k, *v;
+  const int64_t *rows; /* flat (b, kvh, r) ids over [B, Hkv, nq], or NULL for all */
+  int64_t nrows;
+  double *out;   /* [nrows, g, d], or NULL */
+  int32_t *idx;  /* [nrows, 1+W+k], or NULL */
+  int64_t next;
+  pthread_mutex_t mu;
+} orc_gjob;
+
+static void orc_group_row(orc_gjob *J, int64_t slot, int64_t flat, float *shat, double *s64,
+                          orc_cand *cand, unsigned char *inC, float *q32, float *k32) {
+  const orc_params *P = J->P;
+  const int d = P->d;
+  const int64_t g = P->Hq / P->Hkv;
+  const int64_t r = flat % P->nq;
+  const int64_t kvh = (flat / P->nq) % P->Hkv;
+  const int64_t b = flat / (P->nq * P->Hkv);
+  const int64_t p = P->n - P->nq + r;
+  const int64_t W = P->W, K = P->k;
+  const int64_t cmax = 1 + W + K;
+  const double scale = (double)P->scale;
+  const int64_t kbase = (b * P->Hkv + kvh) * P->kv_stride;
+
+  /* group score of every causal position: the largest of the heads' scores */
+  for (int64_t j = 0; j <= p; ++j) shat[j] = -INFINITY;
+  for (int64_t hh = 0; hh < g; ++hh) {
+    const int64_t h = kvh * g + hh;
+    const int64_t qoff = ((b * P->Hq + h) * P->nq + r) * d;
+    for (int c = 0; c < d; ++c) q32[c] = orc_elem(J->q, P->dtype, qoff + c);
+    for (int64_t j = 0; j <= p; ++j) {
+      const int64_t off = (kbase + j) * d;
+      for (int c = 0; c < d; ++c) k32[c] = orc_elem(J->k, P->dtype, off + c);
+      const float s = orc_score_f32(q32, k32, d);
+      if (s > shat[j]) shat[j] = s;
+    }
+  }
+
+  /* anchor + window, then the top-k of 1..p-W by the group score */
+  memset(inC, 0, (size_t)(p + 1));
+  inC[0] = 1;
+  const int64_t wlo = (p - W + 1 > 0) ? p - W + 1 : 0;
+  for (int64_t j = wlo; j <= p; ++j) inC[j] = 1;
+  int64_t nc = 0;
+  for (int64_t j = 1; j <= p - W; ++j) {
+    cand[nc].s = shat[j];
+    cand[nc].j = j;
+    ++nc;
+  }
+  qsort(cand, (size_t)nc, sizeof(orc_cand), orc_cand_cmp);
+  const int64_t take = nc < K ? nc : K;
+  for (int64_t t = 0; t < take; ++t) inC[cand[t].j] = 1;
+
+  if (J->idx) {
+    int32_t *row = J->idx + slot * cmax;
+    int64_t m = 0;
+    for (int64_t j = 0; j <= p; ++j)
+      if (inC[j]) row[m++] = (int32_t)j;
+    for (; m < cmax; ++m) row[m] = -1;
+  }
+
+  /* each head: float64 softmax over the shared set and the weighted sum of V */
+  if (J->out) {
+    for (int64_t hh = 0; hh < g; ++hh) {
+      const int64_t h = kvh * g + hh;
+      const int64_t qoff = ((b * P->Hq + h) * P->nq + r) * d;
+      double mx = -INFINITY;
+      for (int64_t j = 0; j <= p; ++j) {
+        s64[j] = -INFINITY;
+        if (!inC[j]) continue;
+        const int64_t off = (kbase + j) * d;
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+          acc += (double)orc_elem(J->q, P->dtype, qoff + c) *
+                 (double)orc_elem(J->k, P->dtype, off + c);
+        s64[j] = scale * acc;
+        if (s64[j] > mx) mx = s64[j];
+      }
+      double Z = 0.0;
+      double *o = J->out + (slot * g + hh) * d;
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (int64_t j = 0; j <= p; ++j) {
+        if (!inC[j]) continue;
+        const double w = exp(s64[j] - mx);
+        Z += w;
+        const int64_t off = (kbase + j) * d;
+        for (int c = 0; c < d; ++c) o[c] += w * (double)orc_elem(J->v, P->dtype, off + c);
+      }
+      for (int c = 0; c < d; ++c) o[c] /= Z;
+    }
+  }
+}
+
+static void *orc_gworker(void *arg) {
+  orc_gjob *J = (orc_gjob *)arg;
+  const int64_t n = J->P->n, d = J->P->d;
+  float *shat = (float *)malloc(sizeof(float) * (size_t)n);
+  double *s64 = (double *)malloc(sizeof(double) * (size_t)n);
+  orc_cand *cand = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)n);
+  unsigned char *inC = (unsigned char *)malloc((size_t)n);
+  float *q32 = (float *)malloc(sizeof(float) * (size_t)d);
+  float *k32 = (float *)malloc(sizeof(float) * (size_t)d);
+  if (shat && s64 && cand && inC && q32 && k32) {
+    for (;;) {
+      pthread_mutex_lock(&J->mu);
+      const int64_t slot = J->next++;
+      pthread_mutex_unlock(&J->mu);
+      if (slot >= J->nrows) break;
+      const int64_t flat = J->rows ? J->rows[slot] : slot;
+      orc_group_row(J, slot, flat, shat, s64, cand, inC, q32, k32);
+    }
+  }
+  free(shat); free(s64); free(cand); free(inC); free(q32); free(k32);
+  return NULL;
+}
+
+/*
+ * Group-shared condensate-set attention for the listed group rows (all when
+ * rows == NULL); a row id is flat over [B, Hkv, nq].  out: [nrows, g, d]
+ * (head hh of the group at [slot, hh]); idx: [nrows, 1+W+k].  Either may be
+ * NULL.  Returns 0, or -1 on bad arguments.
+ */
+int orc_topo_attn_group(const orc_params *P, const void *q, const void *k, const void *v,
+                        const int64_t *rows, int64_t nrows, double *out, int32_t *idx,
+                        int nthreads) {
+  if (orc_check(P)) return -1;
+  orc_gjob J;
+  memset(&J, 0, sizeof J);
+  J.P = P; J.q = q; J.k = k; J.v = v;
+  J.rows = rows;
+  J.nrows = rows ? nrows : (int64_t)P->B * P->Hkv * P->nq;
+  J.out = out; J.idx = idx;
+  pthread_mutex_init(&J.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 512) nthreads = 512;
+  if (nthreads > J.nrows) nthreads = (int)(J.nrows > 0 ? J.nrows : 1);
+  pthread_t th[512];
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t)
+    if (pthread_create(&th[started], NULL, orc_gworker, &J) == 0) ++started;
+  orc_gworker(&J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&J.mu);
+  return 0;
+}
