@@ -25,7 +25,8 @@ import threading
 
 import torch
 
-__all__ = ["forward", "forward_noalloc", "score_select", "sparse_softmax_pv", "dense_forward",
+__all__ = ["forward", "forward_grouped", "forward_noalloc", "score_select", "sparse_softmax_pv",
+           "dense_forward",
            "layer_schedule", "layers_forward", "Workspace", "TopoError", "library_path",
            "load_library", "workspace_size", "dense_workspace_size", "device_status", "EXPORTS"]
 
@@ -39,7 +40,8 @@ EXPORTS = ("topo_attn_workspace_size", "dense_attn_workspace_size", "topo_attn_w
            "topo_attn_forward", "topo_attn_score_select", "topo_attn_sparse_softmax_pv",
            "dense_attn_forward", "topo_attn_strerror", "topo_attn_device_status",
            "topo_attn_forward_noalloc", "topo_attn_layer_schedule",
-           "topo_attn_layers_workspace_size", "topo_attn_layers_forward")
+           "topo_attn_layers_workspace_size", "topo_attn_layers_forward",
+           "topo_attn_forward_grouped")
 
 TOPO_OK = 0
 TOPO_KMAX = 256
@@ -96,6 +98,7 @@ def load_library():
                                              ctypes.c_int32, vp]),
             "topo_attn_layers_workspace_size": (sz, [P, vp, ctypes.c_int32]),
             "topo_attn_layers_forward": (i, [P, vp, ctypes.c_int32, vp, sz, vp]),
+            "topo_attn_forward_grouped": (i, [P, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -236,6 +239,33 @@ def forward(q, k, v, *, W: int, topk: int, n: int | None = None, scale: float | 
                                    ws.nbytes, _stream(stream, q.device))
     _raise(rc, "topo_attn_forward")
     return out, idx, excl
+
+
+def forward_grouped(q, k, v, *, W: int, topk: int, n: int | None = None,
+                    scale: float | None = None, want_idx: bool = False, out=None, idx=None,
+                    workspace: Workspace | None = None, stream=None):
+    """Group-shared condensate-set attention: one set per (sequence, KV head,
+    row) shared by the KV head's query heads (top-k by the largest of their
+    scores).  Returns (out [B, Hq, nq, d], idx [B, Hkv, nq, 1+W+k] or None)."""
+    _check(q, k, v)
+    lib = load_library()
+    p = make_params(q, k, W=W, topk=topk, n=n, scale=scale)
+    B, Hq, nq, d = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, nq, d), dtype=torch.float32, device=q.device)
+    if want_idx and idx is None:
+        idx = torch.empty((B, k.shape[1], nq, 1 + W + topk), dtype=torch.int32, device=q.device)
+    need = workspace_size(p)
+    if need == 0:
+        _raise(-1 if p.d in (64, 128) else -2, "topo_attn_workspace_size")
+    ws = _workspace(workspace, q.device, need, stream)
+    with torch.cuda.device(q.device):
+        rc = lib.topo_attn_forward_grouped(ctypes.byref(p), q.data_ptr(), k.data_ptr(),
+                                           v.data_ptr(), out.data_ptr(),
+                                           idx.data_ptr() if idx is not None else None,
+                                           ws.ptr, ws.nbytes, _stream(stream, q.device))
+    _raise(rc, "topo_attn_forward_grouped")
+    return out, idx
 
 
 def score_select(q, k, *, W: int, topk: int, n: int | None = None, scale: float | None = None,

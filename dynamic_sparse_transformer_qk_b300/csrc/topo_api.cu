@@ -387,12 +387,16 @@ int dispatch(bool bf16, int D, F&& f) {
   return to_status(f(topo::Launcher<false, 64>()));
 }
 
-// The select pass (and, with excl, the excluded-mass pass).
+// The select pass (and, with excl, the excluded-mass pass).  `group`: one
+// condensate set per (sequence, KV head, row) shared by the KV head's query
+// heads (tensor-core decode shapes only; no excluded mass).
 int run_topo(const topo_attn_params* p, const void* q, const void* k, const void* v, float* out,
-             int32_t* idx, float* excl, void* ws, size_t ws_bytes, cudaStream_t st) {
+             int32_t* idx, float* excl, void* ws, size_t ws_bytes, cudaStream_t st,
+             bool group = false) {
   Plan P;
   int rc = make_plan_cached(p, false, &P);
   if (rc != TOPO_OK) return rc;
+  if (group && (!P.tc || p->Hq / p->Hkv < 2 || excl)) return TOPO_ERR_UNSUPPORTED;
   if (!q || !k) return TOPO_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || (v && !aligned16(v))) return TOPO_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < P.total)
@@ -448,8 +452,9 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
     CUtensorMap mk128;
     rc = make_map(&mk128, k, p, topo::kTcTile);
     if (rc != TOPO_OK) return rc;
-    rc = dispatch(P.bf16, P.D,
-                  [&](auto L) { return L.select_tc(P.NC, P.KE, mk128, G, grid, P.smem, st); });
+    rc = dispatch(P.bf16, P.D, [&](auto L) {
+      return L.select_tc(P.NC, P.KE, group, mk128, G, grid, P.smem, st);
+    });
   } else {
     rc = dispatch(P.bf16, P.D,
                   [&](auto L) { return L.select(P.NC, P.KE, mk, G, grid, P.smem, st); });
@@ -489,6 +494,14 @@ int topo_attn_forward(const topo_attn_params* p, const void* q, const void* k, c
                       topo_stream_t stream) {
   if (!out || !v) return TOPO_ERR_INVALID_ARG;
   return run_topo(p, q, k, v, out, idx, excl, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topo_attn_forward_grouped(const topo_attn_params* p, const void* q, const void* k,
+                              const void* v, float* out, int32_t* idx, void* ws, size_t ws_bytes,
+                              topo_stream_t stream) {
+  if (!out || !v) return TOPO_ERR_INVALID_ARG;
+  return run_topo(p, q, k, v, out, idx, nullptr, ws, ws_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int topo_attn_score_select(const topo_attn_params* p, const void* q, const void* k, int32_t* idx,

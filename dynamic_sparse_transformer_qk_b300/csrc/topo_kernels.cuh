@@ -529,7 +529,12 @@ __device__ __forceinline__ void warp_softmax_pv(const Geom& G, long long kvrow0,
 // weighted sum of V.  Otherwise the lists are read in chunks and one warp per
 // column reads its rows from global memory.  All threads of the CTA call this;
 // warps 0..NW-1 do the per-column work.
-template <bool BF16, int D, int NC, int KE, int NW>
+//
+// GROUP: the lists are per selection column s (one per row of the block, for
+// the g heads col = s*g .. s*g+g-1, see topo_select_tc_kernel); after the
+// merge every column takes its row's list, one idx row per (KV head, row) is
+// written, and the top-k rows are staged once per row.
+template <bool BF16, int D, int NC, int KE, int NW, bool GROUP = false>
 __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nsplit, int b, int kvh,
                                          const ColInfo* cols, const float2* qd, uint64_t* run,
                                          uint8_t* scratch, int scratch_bytes) {
@@ -543,6 +548,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   const int kk = G.topk;
   const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
   const long long cmax = 1 + (long long)G.W + kk;
+  const int nsel = GROUP ? NC / G.g : NC;  // selection columns
 
   // fixed part of the scratch
   int* topj_all = reinterpret_cast<int*>(scratch);                       // [NC][KP]
@@ -601,8 +607,8 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[1]);
     }
     if (!mbar_wait(&bars[0], 0) && tid == 0) set_status(G.status, kStatusTimeout);
-    for (int h = warp; h < NC; h += NW) {
-      if (!cols[h].active) continue;
+    for (int h = warp; h < nsel; h += NW) {
+      if (!cols[GROUP ? h * G.g : h].active) continue;
       const uint64_t* lb = reinterpret_cast<const uint64_t*>(scratch + v0);
       uint64_t a[KE];
 #pragma unroll
@@ -628,8 +634,8 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       const int total = (s1 - s0) * per_split;
       for (int i = tid; i < total; i += blockDim.x) lbuf[i] = __ldcg(src + i);
       __syncthreads();
-      for (int h = warp; h < NC; h += NW) {
-        if (!cols[h].active) continue;
+      for (int h = warp; h < nsel; h += NW) {
+        if (!cols[GROUP ? h * G.g : h].active) continue;
         uint64_t a[KE];
 #pragma unroll
         for (int e = 0; e < KE; ++e) a[e] = run[h * KP + e * 32 + lane];
@@ -644,6 +650,24 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       }
       __syncthreads();
     }
+  }
+
+  if constexpr (GROUP) {
+    // every column takes its row's merged list (read all, then write)
+    constexpr int PER = (NC * KP + 255) / 256;
+    uint64_t tmp[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = tid + q * blockDim.x;
+      tmp[q] = i < NC * KP ? run[((i / KP) / G.g) * KP + i % KP] : 0ull;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = tid + q * blockDim.x;
+      if (i < NC * KP) run[i] = tmp[q];
+    }
+    __syncthreads();
   }
 
   // per column: the k-th key, the selected positions (ascending) and C_i
@@ -672,12 +696,15 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
     for (int e = 0; e < KE; ++e) topj[e * 32 + lane] = y[e] ? (int)(~0ull - y[e]) : -1;
     if (lane == 0) tcount[h] = t;
     __syncwarp();
-    if (G.flags & kDoIdx) {
+    if ((G.flags & kDoIdx) && (!GROUP || h % G.g == 0)) {
       const long long p = cols[h].pos;
       const bool wide = p - G.W + 1 <= 0;  // the window reaches the anchor
       const long long mEnt = wide ? p + 1 : 1 + t + G.W;
       const long long wlo = p - G.W + 1;
-      int* dst = G.idx + cols[h].row * cmax;
+      // one row per (sequence, KV head, row) in group mode
+      const long long irow = GROUP ? ((long long)b * G.Hkv + kvh) * G.nq + (p - (G.n - G.nq))
+                                   : cols[h].row;
+      int* dst = G.idx + irow * cmax;
       for (long long e = lane; e < cmax; e += 32) {
         long long v = -1;
         if (e < mEnt) v = wide ? e : (e == 0 ? 0 : (e <= t ? topj[e - 1] : wlo + (e - 1 - t)));
@@ -718,11 +745,11 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   {
     long long tbytes = 0;
     for (int h = 0; h < NC; ++h)
-      if (cols[h].active) tbytes += (long long)tcount[h] * 2 * S::ROWB;
+      if (cols[h].active && (!GROUP || h % G.g == 0)) tbytes += (long long)tcount[h] * 2 * S::ROWB;
     if (tid == 0) mbar_arrive_expect_tx(&bars[2], (uint32_t)tbytes);
     for (long long sl = tid; sl < (long long)NC * kk; sl += blockDim.x) {
       const int h = (int)(sl / kk), i = (int)(sl % kk);
-      if (!cols[h].active || i >= tcount[h]) continue;
+      if (!cols[h].active || i >= tcount[h] || (GROUP && h % G.g != 0)) continue;
       const long long row = topj_all[h * KP + i];
       uint8_t* dst = stage + (size_t)(top0 + sl) * SLOT;
       bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[2]);
@@ -755,7 +782,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
     long long sl;
     if (p - W + 1 <= 0) sl = e - band_lo;  // 0..p lies in the band, which starts at 0
     else if (e == 0) sl = anchor_slot;
-    else if (e <= t) sl = top0 + (long long)h * kk + (e - 1);
+    else if (e <= t) sl = top0 + (long long)(GROUP ? h - h % G.g : h) * kk + (e - 1);
     else sl = (p - W + 1) + (e - 1 - t) - band_lo;
     slot_tab[i] = (int)sl;
     lw[i] = scale * score_row_smem<BF16, D, NC>(stage + (size_t)sl * SLOT, qd, h);

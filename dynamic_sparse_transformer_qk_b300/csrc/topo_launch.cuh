@@ -24,8 +24,8 @@ struct Launcher {
   static cudaError_t dense(int NC, const CUtensorMap& mk, const CUtensorMap& mv, const Geom& G,
                            dim3 grid, int smem, cudaStream_t st);
   static cudaError_t pv(const Geom& G, long long nrows, cudaStream_t st);
-  static cudaError_t select_tc(int NC, int KE, const CUtensorMap& mk128, const Geom& G, dim3 grid,
-                               int smem, cudaStream_t st);
+  static cudaError_t select_tc(int NC, int KE, bool group, const CUtensorMap& mk128,
+                               const Geom& G, dim3 grid, int smem, cudaStream_t st);
   // chunked prefill on the tensor cores (bf16 only): K scale, scan, finalize, softmax
   static cudaError_t prefill(const CUtensorMap& mk128, const Geom& G, int scan_grid, int scan_smem,
                              int kmax_grid, bool do_pv, cudaStream_t st);
@@ -115,37 +115,46 @@ cudaError_t Launcher<BF16, D>::pv(const Geom& G, long long nrows, cudaStream_t s
   return cudaGetLastError();
 }
 
-template <int D, int NC, int KE>
+template <int D, int NC, int KE, bool GROUP>
 cudaError_t run_select_tc(const CUtensorMap& mk, const Geom& G, dim3 grid, int smem,
                           cudaStream_t st) {
-  constexpr auto kern = &topo_select_tc_kernel<D, NC, KE>;
+  constexpr auto kern = &topo_select_tc_kernel<D, NC, KE, GROUP>;
   const cudaError_t e = allow_smem<kern>();
   if (e != cudaSuccess) return e;
   kern<<<grid, kTcThreads, smem, st>>>(mk, G);
   return cudaGetLastError();
 }
 
-template <int D, int NC>
+template <int D, int NC, bool GROUP>
 cudaError_t run_select_tc_ke(int KE, const CUtensorMap& mk, const Geom& G, dim3 grid, int smem,
                              cudaStream_t st) {
-  if (KE == 1) return run_select_tc<D, NC, 1>(mk, G, grid, smem, st);
+  if (KE == 1) return run_select_tc<D, NC, 1, GROUP>(mk, G, grid, smem, st);
   if constexpr (NC <= 4) {
-    if (KE == 2) return run_select_tc<D, NC, 2>(mk, G, grid, smem, st);
+    if (KE == 2) return run_select_tc<D, NC, 2, GROUP>(mk, G, grid, smem, st);
   }
   return cudaErrorInvalidValue;
 }
 
 template <bool BF16, int D>
-cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, const CUtensorMap& mk128, const Geom& G,
-                                         dim3 grid, int smem, cudaStream_t st) {
+cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, bool group, const CUtensorMap& mk128,
+                                         const Geom& G, dim3 grid, int smem, cudaStream_t st) {
   if constexpr (!BF16) {
     return cudaErrorInvalidValue;
   } else {
+    if (group) {
+      // group-shared selection: at least two heads per selection column
+      switch (NC) {
+        case 2: return run_select_tc_ke<D, 2, true>(KE, mk128, G, grid, smem, st);
+        case 4: return run_select_tc_ke<D, 4, true>(KE, mk128, G, grid, smem, st);
+        case 8: return run_select_tc_ke<D, 8, true>(KE, mk128, G, grid, smem, st);
+        default: return cudaErrorInvalidValue;
+      }
+    }
     switch (NC) {
-      case 1: return run_select_tc_ke<D, 1>(KE, mk128, G, grid, smem, st);
-      case 2: return run_select_tc_ke<D, 2>(KE, mk128, G, grid, smem, st);
-      case 4: return run_select_tc_ke<D, 4>(KE, mk128, G, grid, smem, st);
-      case 8: return run_select_tc_ke<D, 8>(KE, mk128, G, grid, smem, st);
+      case 1: return run_select_tc_ke<D, 1, false>(KE, mk128, G, grid, smem, st);
+      case 2: return run_select_tc_ke<D, 2, false>(KE, mk128, G, grid, smem, st);
+      case 4: return run_select_tc_ke<D, 4, false>(KE, mk128, G, grid, smem, st);
+      case 8: return run_select_tc_ke<D, 8, false>(KE, mk128, G, grid, smem, st);
       default: return cudaErrorInvalidValue;
     }
   }

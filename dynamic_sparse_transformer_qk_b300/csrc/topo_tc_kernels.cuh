@@ -185,7 +185,16 @@ __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, float (&v)[16])
 // Grid and workspace as topo_select_kernel (grid.x = column block x split,
 // grid.y = KV head, grid.z = sequence); a split is G.L keys (a multiple of
 // 128).  bf16 only; k <= 32 * KE, KE <= 2; NC <= 8 / KE columns per block.
-template <int D, int NC, int KE>
+//
+// GROUP: group-shared selection (grouped-query attention).  The block's
+// columns are (row, head) pairs, col = row * g + head; the g heads of a row
+// share one condensate set, whose top-k ranks key j by the largest of the
+// heads' float32 scores.  Selection runs on "selection columns" s = col / g
+// (one per row): the epilogue offers max over the group's tensor-core scores
+// (each within delta_h of its exact score, so the max is within max_h
+// delta_h of the exact max), survivors are rescored as the max of the heads'
+// exact chains, and the tail gives every head of the row the row's set.
+template <int D, int NC, int KE, bool GROUP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     topo_select_tc_kernel(const __grid_constant__ CUtensorMap map_k, const Geom G) {
   using S = Shape<true, D>;
@@ -339,6 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int cnt[NC];
     bool ovf[NC];
     long long jh[NC];
+    const int gsz = GROUP ? G.g : 1;  // heads per selection column
 #pragma unroll
     for (int h = 0; h < NC; ++h) {
       float a = 0.f;
@@ -349,6 +359,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       cnt[h] = 0;
       ovf[h] = false;
       jh[h] = cols[h].active ? (cols[h].jhi < ke ? cols[h].jhi : ke) : 0;
+    }
+    if constexpr (GROUP) {
+      // selection column s covers columns s*g .. s*g+g-1: the largest
+      // coefficient of its heads bounds the error of the max
+#pragma unroll
+      for (int h = 0; h < NC; ++h) {
+        if (h % gsz != 0) continue;
+        float cm = coef[h];
+#pragma unroll
+        for (int i = 1; i < NC; ++i)
+          if (i < gsz && h + i < NC) cm = fmaxf(cm, coef[h + i]);
+        coef[h / gsz] = cm;
+        jh[h / gsz] = jh[h];
+      }
     }
     float kmag = 0.f;  // largest |k_c| seen by this warp
     for (int t = half; t < ntiles; t += 2) {
@@ -367,6 +391,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld_cols<NL>(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(s * kTcColsPerStage),
                        sc);
       tc::tmem_ld_wait();
+      if constexpr (GROUP) {
+        // selection column h: the largest score of its heads
+#pragma unroll
+        for (int h = 0; h < NC; ++h) {
+          if (h * gsz >= NC) continue;
+          float m = sc[h * gsz];
+#pragma unroll
+          for (int i = 1; i < NC; ++i)
+            if (i < gsz && h * gsz + i < NC) m = fmaxf(m, sc[h * gsz + i]);
+          sc[h] = m;
+        }
+      }
       const long long j = ks + (long long)t * kTcTile + r;
       const float mk = j <= ke ? row_magnitude<true, D>(ring + (size_t)s * TILEB, r) : 0.f;
       tc::fence_before_sync();
@@ -381,6 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
 #pragma unroll
       for (int h = 0; h < NC; ++h) {
+        if (GROUP && h * gsz >= NC) continue;
         const bool cand = j <= jh[h];
         bool flag = cand && sc[h] >= thr[h];
         unsigned mask = __ballot_sync(kFull, flag);
@@ -405,7 +442,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // final compaction: each buffer keeps its sorted survivors at [0, LL)
 #pragma unroll 1
-    for (int h = 0; h < NC; ++h) {
+    for (int h = 0; h < (GROUP ? NC / gsz : NC); ++h) {
       uint64_t* hb = mybuf + h * CAP;
       // A buffer of at most 64 entries sorts in half the network; that
       // rewrites (and zero-fills) only slots 0..63, so it is used only when
@@ -435,7 +472,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   // ---------------- per column: exact top-k of this split ----------------
-  for (int h = warp - 2; h >= 0 && h < NC; h += kTcEpiWarps) {
+  const int nsel = GROUP ? NC / G.g : NC;
+  // the exact score of a selection column: one head's chain, or the largest
+  // of the group's heads' chains
+  auto exact_score = [&](long long row, int h) -> float {
+    if constexpr (GROUP) {
+      float m = score_row_global<true, D, NC>(G.kp, row, qd, h * G.g);
+      for (int i = 1; i < G.g; ++i)
+        m = fmaxf(m, score_row_global<true, D, NC>(G.kp, row, qd, h * G.g + i));
+      return m;
+    } else {
+      return score_row_global<true, D, NC>(G.kp, row, qd, h);
+    }
+  };
+  for (int h = warp - 2; h >= 0 && h < nsel; h += kTcEpiWarps) {
     uint64_t a[LE];
 #pragma unroll
     for (int ee = 0; ee < LE; ++ee) a[ee] = wbuf[(size_t)h * CAP + ee * 32 + lane];
@@ -466,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         x[ee] = 0ull;
         if (key != 0ull && key_score(key) >= cut) {
           const uint32_t jj = key_pos(key);
-          x[ee] = rank_key(score_row_global<true, D, NC>(G.kp, kvrow0 + jj, qd, h), jj);
+          x[ee] = rank_key(exact_score(kvrow0 + jj, h), jj);
         }
       }
       warp_sort_desc<LE>(x, lane);
@@ -475,13 +525,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr int FEC = cap_for(KE) / 32;
       uint64_t fthr = 0ull;
       int fcnt = 0;
-      const long long lim = cols[h].active ? (cols[h].jhi < ke ? cols[h].jhi : ke) : 0;
+      const int hc = GROUP ? h * G.g : h;  // a column of the selection column
+      const long long lim = cols[hc].active ? (cols[hc].jhi < ke ? cols[hc].jhi : ke) : 0;
       for (long long j0 = ks; j0 <= lim; j0 += 32) {
         const long long j = j0 + lane;
-        const uint64_t key =
-            j <= lim ? rank_key(score_row_global<true, D, NC>(G.kp, kvrow0 + j, qd, h),
-                                (uint32_t)j)
-                     : 0ull;
+        const uint64_t key = j <= lim ? rank_key(exact_score(kvrow0 + j, h), (uint32_t)j) : 0ull;
         offer<FEC, KE>(scratch, fthr, fcnt, key, kk, lane);
       }
       __syncwarp();
@@ -499,16 +547,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
     for (int ee = 0; ee < KE; ++ee) {
       const int i = ee * 32 + lane;
-      dst[i] = (i < kk && cols[h].active) ? x[ee] : 0ull;
+      const int hc = GROUP ? h * G.g : h;
+      dst[i] = (i < kk && cols[hc].active) ? x[ee] : 0ull;
       // the V rows the final softmax may gather, on their way to L2
-      if (i < kk && cols[h].active && x[ee] != 0ull && G.vp)
+      if (i < kk && cols[hc].active && x[ee] != 0ull && G.vp)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(
             reinterpret_cast<const uint8_t*>(G.vp) + (kvrow0 + key_pos(x[ee])) * S::ROWB));
     }
   }
   if (!finish_split(G.counters + unit, nsplit, misc)) return;
-  select_tail<true, D, NC, KE, kTcWarps>(G, unit, nsplit, b, kvh, cols, qd, wbuf, ring,
-                                         stages * TILEB);
+  select_tail<true, D, NC, KE, kTcWarps, GROUP>(G, unit, nsplit, b, kvh, cols, qd, wbuf, ring,
+                                                stages * TILEB);
 }
 
 }  // namespace topo

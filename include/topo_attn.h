@@ -123,6 +123,26 @@ int topo_attn_forward(const topo_attn_params *p, const void *q, const void *k, c
                       float *out, int32_t *idx, float *excl, void *ws, size_t ws_bytes,
                       topo_stream_t stream);
 
+/*
+ * Group-shared condensate-set attention for grouped-query attention models
+ * (the method is validated on GQA architectures [fr S4]; the pages give no
+ * rule for sharing, this is the reading this library takes): one condensate
+ * set per (sequence, KV head, query row), shared by the Hq/Hkv query heads
+ * that read that KV head.  Its top-k ranks key j by the largest of those
+ * heads' float32 ranking scores (ties to the lower index); anchor and window
+ * as for topo_attn_forward.  Each head then takes its own float32 softmax
+ * over the shared set.  One selection per group instead of per head, and the
+ * selected K/V rows are gathered once per group.
+ *   out : required, [B, Hq, nq, d] float32.
+ *   idx : optional, [B, Hkv, nq, 1+W+k] int32 (one row per group).
+ * Workspace: topo_attn_workspace_size(p).  Supported: bf16, Hq/Hkv >= 2,
+ * nq * Hq/Hkv <= 8 (<= 4 when k > 32), 1 <= k <= 64 (the tensor-core decode
+ * shapes); otherwise TOPO_ERR_UNSUPPORTED.
+ */
+int topo_attn_forward_grouped(const topo_attn_params *p, const void *q, const void *k,
+                              const void *v, float *out, int32_t *idx, void *ws,
+                              size_t ws_bytes, topo_stream_t stream);
+
 /* The scoring and selection steps alone [fr S2, ko S3]: writes idx (required). */
 int topo_attn_score_select(const topo_attn_params *p, const void *q, const void *k,
                            int32_t *idx, void *ws, size_t ws_bytes, topo_stream_t stream);

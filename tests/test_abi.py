@@ -165,3 +165,16 @@ def test_layers_forward_checks_every_layer_first(lib):
     # a pillar layer ignores W and k: a bad W there is not an error
     arr[1].W = -5
     assert lib.topo_attn_layers_workspace_size(ctypes.byref(p), a, 3) == need
+
+
+def test_grouped_rejects_unsupported_shapes(lib):
+    need = 1 << 30
+    # float32, one head per group, prefill-sized column counts: not the grouped shapes
+    for bad in (dict(dtype=0), dict(Hq=8, Hkv=8), dict(nq=64)):
+        p = _p(**bad)
+        rc = lib.topo_attn_forward_grouped(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                           need, None)
+        assert rc == -2, bad
+    p = _p()
+    assert lib.topo_attn_forward_grouped(ctypes.byref(p), FAKE, FAKE, None, FAKE, None, FAKE,
+                                         need, None) == -1
