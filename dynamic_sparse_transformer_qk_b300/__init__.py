@@ -26,7 +26,7 @@ import threading
 import torch
 
 __all__ = ["forward", "forward_grouped", "forward_noalloc", "score_select", "sparse_softmax_pv",
-           "dense_forward",
+           "dense_forward", "compact_kv",
            "layer_schedule", "layers_forward", "Workspace", "TopoError", "library_path",
            "load_library", "workspace_size", "dense_workspace_size", "device_status", "EXPORTS"]
 
@@ -41,7 +41,7 @@ EXPORTS = ("topo_attn_workspace_size", "dense_attn_workspace_size", "topo_attn_w
            "dense_attn_forward", "topo_attn_strerror", "topo_attn_device_status",
            "topo_attn_forward_noalloc", "topo_attn_layer_schedule",
            "topo_attn_layers_workspace_size", "topo_attn_layers_forward",
-           "topo_attn_forward_grouped")
+           "topo_attn_forward_grouped", "topo_attn_compact_kv")
 
 TOPO_OK = 0
 TOPO_KMAX = 256
@@ -99,6 +99,7 @@ def load_library():
             "topo_attn_layers_workspace_size": (sz, [P, vp, ctypes.c_int32]),
             "topo_attn_layers_forward": (i, [P, vp, ctypes.c_int32, vp, sz, vp]),
             "topo_attn_forward_grouped": (i, [P, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "topo_attn_compact_kv": (i, [P, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -307,6 +308,33 @@ def sparse_softmax_pv(q, k, v, idx, *, W: int, topk: int, n: int | None = None,
                                              _stream(stream, q.device))
     _raise(rc, "topo_attn_sparse_softmax_pv")
     return out
+
+
+def compact_kv(k, v, idx, *, Hq: int, n: int | None = None, k_out=None, v_out=None,
+               stream=None):
+    """topo_attn_compact_kv: the K and V rows each query row's condensate set
+    names (idx [B, Hq, nq, 1+W+k]), gathered into [B, Hq, nq, 1+W+k, d]
+    (zero rows for -1 entries).  W and k are read off idx: pass the same n."""
+    _check(k, v)
+    lib = load_library()
+    B, Hkv, stride, d = k.shape
+    if idx.dtype != torch.int32 or idx.dim() != 4 or idx.shape[0] != B or idx.shape[1] != Hq \
+            or not idx.is_contiguous() or idx.device != k.device:
+        raise ValueError("idx must be contiguous int32 [B, Hq, nq, 1+W+k] on k's device")
+    nq, cmax = idx.shape[2], idx.shape[3]
+    # only the row length 1 + W + k matters here
+    p = Params(B, Hq, Hkv, d, stride if n is None else n, nq, stride, cmax - 1, 0, 1.0,
+               _dtype_code(k))
+    if k_out is None:
+        k_out = torch.empty((B, Hq, nq, cmax, d), dtype=k.dtype, device=k.device)
+    if v_out is None:
+        v_out = torch.empty((B, Hq, nq, cmax, d), dtype=v.dtype, device=v.device)
+    with torch.cuda.device(k.device):
+        rc = lib.topo_attn_compact_kv(ctypes.byref(p), k.data_ptr(), v.data_ptr(),
+                                      idx.data_ptr(), k_out.data_ptr(), v_out.data_ptr(),
+                                      _stream(stream, k.device))
+    _raise(rc, "topo_attn_compact_kv")
+    return k_out, v_out
 
 
 def dense_forward(q, k, v, *, n: int | None = None, scale: float | None = None, out=None,

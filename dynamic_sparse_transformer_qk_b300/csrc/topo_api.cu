@@ -533,6 +533,25 @@ int topo_attn_sparse_softmax_pv(const topo_attn_params* p, const void* q, const 
   return dispatch(p->dtype == TOPO_BF16, p->d, [&](auto L) { return L.pv(G, nrows, st); });
 }
 
+int topo_attn_compact_kv(const topo_attn_params* p, const void* k, const void* v,
+                         const int32_t* idx, void* k_out, void* v_out, topo_stream_t stream) {
+  const int rc = check_params(p);
+  if (rc != TOPO_OK) return rc;
+  if (!k || !v || !idx || !k_out || !v_out) return TOPO_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
+    return TOPO_ERR_INVALID_ARG;
+  Plan P;
+  P.ncols = p->nq * (p->Hq / p->Hkv);
+  P.ncb = 1;
+  Geom G = base_geom(p, P);
+  G.kp = k;
+  G.vp = v;
+  G.idx = const_cast<int32_t*>(idx);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return dispatch(p->dtype == TOPO_BF16, p->d,
+                  [&](auto L) { return L.compact(G, k_out, v_out, st); });
+}
+
 int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, const void* v,
                        float* out, void* ws, size_t ws_bytes, topo_stream_t stream) {
   Plan P;

@@ -1305,4 +1305,39 @@ __global__ void __launch_bounds__(128) sparse_pv_kernel(const Geom G) {
                               G.out + row * D, lane);
 }
 
+// ================================================ condensate KV compaction ==
+//
+// out[row][e] = rows idx[row][e] of K and V of the row's KV head (zero rows
+// for entries outside 0..n-1).  One warp per (row, entry group of 8): a lane
+// moves 16 bytes of each row.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256) compact_kv_kernel(const Geom G, void* k_out, void* v_out) {
+  using S = Shape<BF16, D>;
+  constexpr int VPR = S::ROWB / 16;  // 16-byte vectors per row
+  const long long cmax = 1 + (long long)G.W + G.topk;
+  const long long nrows = (long long)G.B * G.Hq * G.nq;
+  const long long total = nrows * cmax * VPR;
+  const uint4* kin = reinterpret_cast<const uint4*>(G.kp);
+  const uint4* vin = reinterpret_cast<const uint4*>(G.vp);
+  uint4* ko = reinterpret_cast<uint4*>(k_out);
+  uint4* vo = reinterpret_cast<uint4*>(v_out);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long ent = i / VPR;  // (row, entry)
+    const int vv = (int)(i % VPR);
+    const long long row = ent / cmax;
+    const int h = (int)((row / G.nq) % G.Hq);
+    const int b = (int)(row / (G.nq * G.Hq));
+    const int j = G.idx[ent];
+    uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
+    if (j >= 0 && j < G.n) {
+      const long long src = (((long long)b * G.Hkv + h / G.g) * G.kv_stride + j) * VPR + vv;
+      kx = __ldg(kin + src);
+      vx = __ldg(vin + src);
+    }
+    ko[i] = kx;
+    vo[i] = vx;
+  }
+}
+
 }  // namespace topo

@@ -24,6 +24,7 @@ struct Launcher {
   static cudaError_t dense(int NC, const CUtensorMap& mk, const CUtensorMap& mv, const Geom& G,
                            dim3 grid, int smem, cudaStream_t st);
   static cudaError_t pv(const Geom& G, long long nrows, cudaStream_t st);
+  static cudaError_t compact(const Geom& G, void* k_out, void* v_out, cudaStream_t st);
   static cudaError_t select_tc(int NC, int KE, bool group, const CUtensorMap& mk128,
                                const Geom& G, dim3 grid, int smem, cudaStream_t st);
   // chunked prefill on the tensor cores (bf16 only): K scale, scan, finalize, softmax
@@ -112,6 +113,18 @@ template <bool BF16, int D>
 cudaError_t Launcher<BF16, D>::pv(const Geom& G, long long nrows, cudaStream_t st) {
   const long long blocks = (nrows + 3) / 4;
   sparse_pv_kernel<BF16, D><<<(unsigned)blocks, 128, 0, st>>>(G);
+  return cudaGetLastError();
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::compact(const Geom& G, void* k_out, void* v_out,
+                                       cudaStream_t st) {
+  const long long total = (long long)G.B * G.Hq * G.nq * (1 + (long long)G.W + G.topk) *
+                          (Shape<BF16, D>::ROWB / 16);
+  long long blocks = (total + 255) / 256;
+  if (blocks > 148 * 16) blocks = 148 * 16;  // grid-stride beyond 16 blocks per SM
+  if (blocks < 1) blocks = 1;
+  compact_kv_kernel<BF16, D><<<(unsigned)blocks, 256, 0, st>>>(G, k_out, v_out);
   return cudaGetLastError();
 }
 

@@ -157,6 +157,25 @@ int topo_attn_sparse_softmax_pv(const topo_attn_params *p, const void *q, const 
                                 const void *v, const int32_t *idx, float *out,
                                 topo_stream_t stream);
 
+/*
+ * Condensate KV compaction [zh S4: storing only the condensate set's KV;
+ * ko S4 (2): memory saving].  For each query row, gathers the K and V rows
+ * its condensate set names into a compact cache:
+ *   k_out, v_out [B, Hq, nq, 1+W+k, d]  (dtype of k / v)
+ *   k_out[b,h,r,e] = k[b, h/(Hq/Hkv), idx[b,h,r,e]]  for idx >= 0, zero rows
+ *   where idx is -1.
+ * idx is [B, Hq, nq, 1+W+k] as written by topo_attn_forward /
+ * topo_attn_score_select.  The compact cache is exact for these queries:
+ * their outputs depend only on these rows, so the softmax over the compact
+ * rows (topo_attn_sparse_softmax_pv with entries 0..|C|-1, n = 1+W+k)
+ * reproduces them.  It cannot serve other queries: with dynamic top-k a new
+ * query may select any earlier key, so the full cache stays the source of
+ * truth.  Entries of idx outside 0..n-1 are treated as -1.  Needs no
+ * workspace.
+ */
+int topo_attn_compact_kv(const topo_attn_params *p, const void *k, const void *v,
+                         const int32_t *idx, void *k_out, void *v_out, topo_stream_t stream);
+
 /* Dense causal attention over keys 0..p (the full-attention "pillar" layer,
  * [zh S3]); W and k are ignored. */
 int dense_attn_forward(const topo_attn_params *p, const void *q, const void *k, const void *v,

@@ -178,3 +178,11 @@ def test_grouped_rejects_unsupported_shapes(lib):
     p = _p()
     assert lib.topo_attn_forward_grouped(ctypes.byref(p), FAKE, FAKE, None, FAKE, None, FAKE,
                                          need, None) == -1
+
+
+def test_compact_kv_rejects_bad_arguments(lib):
+    p = _p()
+    assert lib.topo_attn_compact_kv(ctypes.byref(p), FAKE, FAKE, None, FAKE, FAKE, None) == -1
+    assert lib.topo_attn_compact_kv(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE + 4, FAKE, None) == -1
+    assert lib.topo_attn_compact_kv(ctypes.byref(_p(d=96)), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    None) == -2
