@@ -26,7 +26,7 @@ import threading
 import torch
 
 __all__ = ["forward", "forward_grouped", "forward_noalloc", "score_select", "sparse_softmax_pv",
-           "dense_forward", "compact_kv",
+           "dense_forward", "compact_kv", "forward_paged",
            "layer_schedule", "layers_forward", "Workspace", "TopoError", "library_path",
            "load_library", "workspace_size", "dense_workspace_size", "device_status", "EXPORTS"]
 
@@ -41,7 +41,8 @@ EXPORTS = ("topo_attn_workspace_size", "dense_attn_workspace_size", "topo_attn_w
            "dense_attn_forward", "topo_attn_strerror", "topo_attn_device_status",
            "topo_attn_forward_noalloc", "topo_attn_layer_schedule",
            "topo_attn_layers_workspace_size", "topo_attn_layers_forward",
-           "topo_attn_forward_grouped", "topo_attn_compact_kv")
+           "topo_attn_forward_grouped", "topo_attn_compact_kv", "topo_attn_paged_workspace_size",
+           "topo_attn_forward_paged")
 
 TOPO_OK = 0
 TOPO_KMAX = 256
@@ -58,6 +59,13 @@ class Params(ctypes.Structure):
                 ("d", ctypes.c_int32), ("n", ctypes.c_int64), ("nq", ctypes.c_int64),
                 ("kv_stride", ctypes.c_int64), ("W", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class PagedKV(ctypes.Structure):
+    """topo_paged_kv (include/topo_attn.h)."""
+    _fields_ = [("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("max_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("out_bf16", ctypes.c_int32)]
 
 
 class TopoLayer(ctypes.Structure):
@@ -100,6 +108,8 @@ def load_library():
             "topo_attn_layers_forward": (i, [P, vp, ctypes.c_int32, vp, sz, vp]),
             "topo_attn_forward_grouped": (i, [P, vp, vp, vp, vp, vp, vp, sz, vp]),
             "topo_attn_compact_kv": (i, [P, vp, vp, vp, vp, vp, vp]),
+            "topo_attn_paged_workspace_size": (sz, [P, vp]),
+            "topo_attn_forward_paged": (i, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -335,6 +345,56 @@ def compact_kv(k, v, idx, *, Hq: int, n: int | None = None, k_out=None, v_out=No
                                       _stream(stream, k.device))
     _raise(rc, "topo_attn_compact_kv")
     return k_out, v_out
+
+
+def forward_paged(q, k_pool, v_pool, *, W: int, topk: int, n: int, block_table=None,
+                  seq_lens=None, block_size: int = 0, scale: float | None = None,
+                  out_bf16: bool = False, want_idx: bool = False, out=None, idx=None,
+                  workspace: Workspace | None = None, stream=None):
+    """topo_attn_forward_paged: condensate-set attention over a paged KV cache
+    (k_pool, v_pool [num_blocks, Hkv, block_size, d] with block_table
+    [B, max_blocks] int32) or a contiguous one (block_table None), with
+    optional per-sequence lengths seq_lens [B] int32 and a bf16 or float32
+    output.  n: the largest sequence length.  Returns (out, idx or None)."""
+    _check(q, k_pool, v_pool)
+    lib = load_library()
+    B, Hq, nq, d = q.shape
+    Hkv = k_pool.shape[1]
+    paged = block_table is not None
+    kv = PagedKV(None, None, 0, 0, 0, int(out_bf16))
+    if paged:
+        if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+                or not block_table.is_contiguous() or block_table.device != q.device:
+            raise ValueError("block_table must be contiguous int32 [B, max_blocks] on q's device")
+        kv.block_table = block_table.data_ptr()
+        kv.max_blocks = block_table.shape[1]
+        kv.block_size = block_size or k_pool.shape[2]
+        kv.num_blocks = k_pool.shape[0]
+        stride = n
+    else:
+        stride = k_pool.shape[2]
+    if seq_lens is not None:
+        if seq_lens.dtype != torch.int32 or seq_lens.numel() != B or seq_lens.device != q.device:
+            raise ValueError("seq_lens must be int32 [B] on q's device")
+        kv.seq_lens = seq_lens.data_ptr()
+    p = Params(B, Hq, Hkv, d, n, nq, stride, W, topk,
+               scale if scale is not None else 1.0 / math.sqrt(d), _dtype_code(q))
+    if out is None:
+        out = torch.empty((B, Hq, nq, d), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                          device=q.device)
+    if want_idx and idx is None:
+        idx = torch.empty((B, Hq, nq, 1 + W + topk), dtype=torch.int32, device=q.device)
+    need = int(lib.topo_attn_paged_workspace_size(ctypes.byref(p), ctypes.byref(kv)))
+    if need == 0:
+        _raise(-2, "topo_attn_paged_workspace_size")
+    ws = _workspace(workspace, q.device, need, stream)
+    with torch.cuda.device(q.device):
+        rc = lib.topo_attn_forward_paged(ctypes.byref(p), ctypes.byref(kv), q.data_ptr(),
+                                         k_pool.data_ptr(), v_pool.data_ptr(), out.data_ptr(),
+                                         idx.data_ptr() if idx is not None else None, ws.ptr,
+                                         ws.nbytes, _stream(stream, q.device))
+    _raise(rc, "topo_attn_forward_paged")
+    return out, idx
 
 
 def dense_forward(q, k, v, *, n: int | None = None, scale: float | None = None, out=None,

@@ -133,8 +133,10 @@ void ring_shape(int stage_bytes, int fixed_bytes, int min_ring, int* stages, int
   *ncw = *stages < topo::kConsumerWarps ? *stages : topo::kConsumerWarps;
 }
 
-// Plan for the condensate-set passes (dense=false) or the dense pass.
-int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
+// Plan for the condensate-set passes (dense=false) or the dense pass.  A
+// paged cache scans from key 0 (block-aligned tiles), one more key per
+// split range.
+int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false) {
   int rc = check_params(p);
   if (rc != TOPO_OK) return rc;
   P->bf16 = p->dtype == TOPO_BF16;
@@ -160,7 +162,8 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
     P->units = (long long)p->B * p->Hkv;
   }
   if (!dense) {
-    const long long ncand = p->k > 0 ? pos_max - p->W : 0;
+    long long ncand = p->k > 0 ? pos_max - p->W : 0;
+    if (paged && ncand > 0) ncand += 1;
     P->L = P->tc ? choose_split_tc(P->units, ncand > 0 ? ncand : 0, slots, 1200)
                  : choose_split(P->units, ncand > 0 ? ncand : 0, slots);
     P->nsplit = ncand > 0 ? (int)ceil_div(ncand, P->L) : 1;
@@ -264,7 +267,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P) {
 constexpr int kPlanCache = 32;
 struct PlanEntry {
   topo_attn_params p;
-  int dense, dev, rc, valid;
+  int dense, paged, dev, rc, valid;
   Plan plan;
 };
 std::mutex g_plan_mu;
@@ -277,7 +280,7 @@ bool same_params(const topo_attn_params& a, const topo_attn_params& b) {
          memcmp(&a.scale, &b.scale, sizeof a.scale) == 0 && a.dtype == b.dtype;
 }
 
-int make_plan_cached(const topo_attn_params* p, bool dense, Plan* P) {
+int make_plan_cached(const topo_attn_params* p, bool dense, Plan* P, bool paged = false) {
   if (!p) return TOPO_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -288,18 +291,20 @@ int make_plan_cached(const topo_attn_params* p, bool dense, Plan* P) {
     std::lock_guard<std::mutex> lock(g_plan_mu);
     for (int i = 0; i < kPlanCache; ++i) {
       const PlanEntry& e = g_plans[i];
-      if (e.valid && e.dense == (int)dense && e.dev == dev && same_params(e.p, *p)) {
+      if (e.valid && e.dense == (int)dense && e.paged == (int)paged && e.dev == dev &&
+          same_params(e.p, *p)) {
         *P = e.plan;
         return e.rc;
       }
     }
   }
-  const int rc = make_plan(p, dense, P);
+  const int rc = make_plan(p, dense, P, paged);
   std::lock_guard<std::mutex> lock(g_plan_mu);
   PlanEntry& e = g_plans[g_plan_next];
   g_plan_next = (g_plan_next + 1) % kPlanCache;
   e.p = *p;
   e.dense = (int)dense;
+  e.paged = (int)paged;
   e.dev = dev;
   e.rc = rc;
   e.plan = *P;
@@ -322,15 +327,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over the rows of k or v ([B*Hkv*kv_stride, d]); box = 128 bytes of
-// one row x box_rows rows, 128-byte swizzle.
+// 2-D map over the rows of k or v ([B*Hkv*kv_stride, d], or `nrows` rows of
+// a paged pool); box = 128 bytes of one row x box_rows rows, 128-byte swizzle.
 int make_map(CUtensorMap* map, const void* base, const topo_attn_params* p,
-             int box_rows = kTile) {
+             int box_rows = kTile, long long nrows = 0) {
   auto fn = encode_fn();
   if (!fn) return TOPO_ERR_CUDA;
   const bool bf16 = p->dtype == TOPO_BF16;
   const int es = bf16 ? 2 : 4;
-  const cuuint64_t rows = (cuuint64_t)p->B * p->Hkv * p->kv_stride;
+  const cuuint64_t rows = nrows > 0 ? (cuuint64_t)nrows : (cuuint64_t)p->B * p->Hkv * p->kv_stride;
   const cuuint64_t dims[2] = {(cuuint64_t)p->d, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)p->d * es};
   const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
@@ -392,20 +397,32 @@ int dispatch(bool bf16, int D, F&& f) {
 // heads (tensor-core decode shapes only; no excluded mass).
 int run_topo(const topo_attn_params* p, const void* q, const void* k, const void* v, float* out,
              int32_t* idx, float* excl, void* ws, size_t ws_bytes, cudaStream_t st,
-             bool group = false) {
+             bool group = false, const topo_paged_kv* paged = nullptr) {
+  const bool pool = paged && paged->block_table;
   Plan P;
-  int rc = make_plan_cached(p, false, &P);
+  int rc = make_plan_cached(p, false, &P, pool);
   if (rc != TOPO_OK) return rc;
   if (group && (!P.tc || p->Hq / p->Hkv < 2 || excl)) return TOPO_ERR_UNSUPPORTED;
+  if (paged && (!P.tc || excl)) return TOPO_ERR_UNSUPPORTED;
   if (!q || !k) return TOPO_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || (v && !aligned16(v))) return TOPO_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < P.total)
     return TOPO_ERR_WORKSPACE;
+  const long long pool_rows =
+      pool ? (long long)paged->num_blocks * p->Hkv * paged->block_size : 0;
   CUtensorMap mk;
-  rc = make_map(&mk, k, p);
+  rc = make_map(&mk, k, p, kTile, pool_rows);
   if (rc != TOPO_OK) return rc;
   uint8_t* w = static_cast<uint8_t*>(ws);
   Geom G = base_geom(p, P);
+  if (paged) {
+    G.block_table = paged->block_table;
+    G.seq_lens = paged->seq_lens;
+    G.max_blocks = paged->max_blocks;
+    G.block_size = paged->block_size;
+    G.num_blocks = paged->num_blocks;
+    G.out_bf16 = paged->out_bf16 ? 1 : 0;
+  }
   G.qp = q;
   G.kp = k;
   G.vp = v;
@@ -450,7 +467,7 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
     G.thr = reinterpret_cast<unsigned long long*>(w + P.off_thr);
   } else if (P.tc) {
     CUtensorMap mk128;
-    rc = make_map(&mk128, k, p, topo::kTcTile);
+    rc = make_map(&mk128, k, p, topo::kTcTile, pool_rows);
     if (rc != TOPO_OK) return rc;
     rc = dispatch(P.bf16, P.D, [&](auto L) {
       return L.select_tc(P.NC, P.KE, group, mk128, G, grid, P.smem, st);
@@ -494,6 +511,28 @@ int topo_attn_forward(const topo_attn_params* p, const void* q, const void* k, c
                       topo_stream_t stream) {
   if (!out || !v) return TOPO_ERR_INVALID_ARG;
   return run_topo(p, q, k, v, out, idx, excl, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t topo_attn_paged_workspace_size(const topo_attn_params* p, const topo_paged_kv* kv) {
+  Plan P;
+  return make_plan_cached(p, false, &P, kv && kv->block_table) == TOPO_OK ? P.total : 0;
+}
+
+int topo_attn_forward_paged(const topo_attn_params* p, const topo_paged_kv* kv, const void* q,
+                            const void* k_pool, const void* v_pool, void* out, int32_t* idx,
+                            void* ws, size_t ws_bytes, topo_stream_t stream) {
+  if (!kv || !out || !v_pool) return TOPO_ERR_INVALID_ARG;
+  const int rc = check_params(p);
+  if (rc != TOPO_OK) return rc;
+  if (kv->block_table) {
+    if (kv->block_size < topo::kTcTile || kv->block_size % topo::kTcTile || kv->num_blocks < 1 ||
+        kv->max_blocks < 1 || (long long)kv->max_blocks * kv->block_size < p->n)
+      return TOPO_ERR_INVALID_ARG;
+    if ((long long)kv->num_blocks * p->Hkv * kv->block_size > kMaxRows)
+      return TOPO_ERR_UNSUPPORTED;
+  }
+  return run_topo(p, q, k_pool, v_pool, static_cast<float*>(out), idx, nullptr, ws, ws_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), false, kv);
 }
 
 int topo_attn_forward_grouped(const topo_attn_params* p, const void* q, const void* k,
@@ -652,6 +691,8 @@ const char* topo_attn_strerror(int status) {
     case TOPO_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
     case TOPO_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than the no-allocation entry point's fixed buffer";
+    case TOPO_ERR_BAD_BLOCK:
+      return "a block-table entry was outside the pool (the block was read as block 0)";
     default: return "unknown status";
   }
 }

@@ -23,6 +23,8 @@
 //             ever waits on another) combines the splits' partial results.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "topo_device.cuh"
 
 namespace topo {
@@ -65,7 +67,44 @@ struct Geom {
   long long nitems;           // scan work items (blocks of 128 columns)
   int items_per_head;         // blocks per (sequence, KV head)
   int thr_nc;                 // columns per unit of the excluded-mass pass
+  // paged KV (tensor-core decode path): K and V are pools [blocks, Hkv,
+  // block_size, d]; key j of sequence b lives in block
+  // block_table[b * max_blocks + j / block_size].  Null table: contiguous.
+  const int* block_table;
+  const int* seq_lens;        // [B] causal length per sequence (clamped to nq..n), or null
+  int max_blocks, block_size, num_blocks;
+  int out_bf16;               // out holds bfloat16 values instead of float
 };
+
+constexpr int kStatusBadBlock = -7;  // TOPO_ERR_BAD_BLOCK: a block-table entry was out of range
+
+// Row of key j of (sequence b, KV head h) in the K and V arrays: contiguous
+// [B, Hkv, kv_stride] rows, or the paged pool's [blocks, Hkv, block_size]
+// rows through the block table (an out-of-range entry is reported in the
+// status word and read as block 0, so no access leaves the pool).
+__device__ __forceinline__ long long kv_row(const Geom& G, int b, int h, long long j) {
+  if (!G.block_table) return ((long long)b * G.Hkv + h) * G.kv_stride + j;
+  int blk = G.block_table[(long long)b * G.max_blocks + j / G.block_size];
+  if (blk < 0 || blk >= G.num_blocks) {
+    if (G.status) atomicCAS(G.status, 0, kStatusBadBlock);
+    blk = 0;
+  }
+  return ((long long)blk * G.Hkv + h) * G.block_size + j % G.block_size;
+}
+
+// Causal length of sequence b: the per-sequence length when given (clamped
+// to nq..n, so that every query row has a position), else n.
+__device__ __forceinline__ long long seq_len(const Geom& G, int b) {
+  if (!G.seq_lens) return G.n;
+  const long long s = G.seq_lens[b];
+  return s < G.nq ? G.nq : (s > G.n ? G.n : s);
+}
+
+// Store output element i (float, or bf16 when G.out_bf16).
+__device__ __forceinline__ void store_out(const Geom& G, long long i, float x) {
+  if (G.out_bf16) reinterpret_cast<__nv_bfloat16*>(G.out)[i] = __float2bfloat16_rn(x);
+  else G.out[i] = x;
+}
 
 struct ColInfo {
   long long pos;   // absolute position of the query row
@@ -116,6 +155,7 @@ __device__ __forceinline__ uint8_t* aligned_smem_base() {
 template <bool BF16, int D, int NC>
 __device__ void load_columns(const Geom& G, int b, int kvh, long long cb, ColInfo* cols,
                              float2* qd) {
+  const long long nb = seq_len(G, b);
   const int tid = threadIdx.x;
   if (tid < NC) {
     const long long col = cb * NC + tid;
@@ -123,7 +163,7 @@ __device__ void load_columns(const Geom& G, int b, int kvh, long long cb, ColInf
     ci.active = col < G.ncols;
     const long long r = ci.active ? col / G.g : 0;
     const int h = kvh * G.g + (ci.active ? (int)(col % G.g) : 0);
-    ci.pos = G.n - G.nq + r;
+    ci.pos = nb - G.nq + r;
     ci.jhi = ci.active ? ci.pos - G.W : -1;
     ci.row = ((long long)b * G.Hq + h) * G.nq + r;
     ci.pad = 0;
@@ -413,9 +453,10 @@ __device__ __forceinline__ void offer(uint64_t* buf, uint64_t& thr, int& cnt, ui
 // One warp: out = sum_e w_e v_{j(e)} / sum_e w_e over entries e in [0, m) with
 // positions j = entry(e) (negative: skip), w_e = exp(l_e - max l), l_e =
 // scale * (float32 chain q . k_j); float32 online softmax in chunks of 256.
-template <bool BF16, int D, class Entry, class Score>
-__device__ void warp_softmax_pv_with(const Geom& G, long long kvrow0, Score&& score, long long m,
-                                     Entry&& entry, float* wsm, int* jsm, float* outp, int lane) {
+template <bool BF16, int D, class Entry, class Score, class RowOf>
+__device__ void warp_softmax_pv_with(const Geom& G, RowOf&& row_of, Score&& score, long long m,
+                                     Entry&& entry, float* wsm, int* jsm, long long out_off,
+                                     int lane) {
   using S = Shape<BF16, D>;
   float mrun = -INFINITY, Z = 0.f;
   float acc[S::EPL];
@@ -430,11 +471,11 @@ __device__ void warp_softmax_pv_with(const Geom& G, long long kvrow0, Score&& sc
       float l = -INFINITY;
       if (j >= 0) {
         // start the V row on its way to L2 while the logit is computed
-        const uint8_t* vrow = vbase + (kvrow0 + j) * S::ROWB;
+        const uint8_t* vrow = vbase + row_of(j) * S::ROWB;
 #pragma unroll
         for (int o = 0; o < S::ROWB; o += 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + o));
-        l = G.scale * score(kvrow0 + j);
+        l = G.scale * score(row_of(j));
       }
       wsm[i] = l;
       jsm[i] = (int)j;
@@ -465,7 +506,7 @@ __device__ void warp_softmax_pv_with(const Geom& G, long long kvrow0, Score&& sc
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = jsm[i + u];
-        lane_elems<BF16, D>(vbase + (kvrow0 + (j >= 0 ? j : 0)) * S::ROWB + lane * S::BPL, v[u]);
+        lane_elems<BF16, D>(vbase + row_of(j >= 0 ? j : 0) * S::ROWB + lane * S::BPL, v[u]);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -479,14 +520,15 @@ __device__ void warp_softmax_pv_with(const Geom& G, long long kvrow0, Score&& sc
       if (j < 0) continue;
       const float w = wsm[i];
       float v[S::EPL];
-      lane_elems<BF16, D>(vbase + (kvrow0 + j) * S::ROWB + lane * S::BPL, v);
+      lane_elems<BF16, D>(vbase + row_of(j) * S::ROWB + lane * S::BPL, v);
 #pragma unroll
       for (int e = 0; e < S::EPL; ++e) acc[e] = fmaf(w, v[e], acc[e]);
     }
     __syncwarp();
   }
 #pragma unroll
-  for (int e = 0; e < S::EPL; ++e) outp[lane * S::EPL + e] = Z > 0.f ? acc[e] / Z : 0.f;
+  for (int e = 0; e < S::EPL; ++e)
+    store_out(G, out_off + lane * S::EPL + e, Z > 0.f ? acc[e] / Z : 0.f);
 }
 
 // The float32 chain for one key row held in shared memory (linear layout).
@@ -506,13 +548,13 @@ __device__ __forceinline__ float score_row_smem(const uint8_t* krow, const float
 }
 
 template <bool BF16, int D, int NC, class Entry>
-__device__ __forceinline__ void warp_softmax_pv(const Geom& G, long long kvrow0, const float2* qd,
+__device__ __forceinline__ void warp_softmax_pv(const Geom& G, int b, int kvh, const float2* qd,
                                                 int hc, long long m, Entry&& entry, float* wsm,
-                                                int* jsm, float* outp, int lane) {
+                                                int* jsm, long long out_off, int lane) {
   warp_softmax_pv_with<BF16, D>(
-      G, kvrow0,
+      G, [&](long long j) { return kv_row(G, b, kvh, j); },
       [&](long long row) { return score_row_global<BF16, D, NC>(G.kp, row, qd, hc); }, m, entry,
-      wsm, jsm, outp, lane);
+      wsm, jsm, out_off, lane);
 }
 
 // Tail of the select kernels, run by the CTA that finished a column block
@@ -546,7 +588,6 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   constexpr int SLOT = 2 * S::ROWB + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kk = G.topk;
-  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
   const long long cmax = 1 + (long long)G.W + kk;
   const int nsel = GROUP ? NC / G.g : NC;  // selection columns
 
@@ -603,8 +644,9 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       long long row = sl < nb ? band_lo + sl : (band_lo == 0 ? -1 : 0);
       if (row < 0) continue;
       uint8_t* dst = stage + (size_t)sl * SLOT;
-      bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[1]);
-      bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[1]);
+      const long long gr = kv_row(G, b, kvh, row);
+      bulk_copy_g2s(dst, kb + gr * S::ROWB, S::ROWB, &bars[1]);
+      bulk_copy_g2s(dst + S::ROWB, vb + gr * S::ROWB, S::ROWB, &bars[1]);
     }
     if (!mbar_wait(&bars[0], 0) && tid == 0) set_status(G.status, kStatusTimeout);
     for (int h = warp; h < nsel; h += NW) {
@@ -702,8 +744,8 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       const long long mEnt = wide ? p + 1 : 1 + t + G.W;
       const long long wlo = p - G.W + 1;
       // one row per (sequence, KV head, row) in group mode
-      const long long irow = GROUP ? ((long long)b * G.Hkv + kvh) * G.nq + (p - (G.n - G.nq))
-                                   : cols[h].row;
+      const long long irow =
+          GROUP ? ((long long)b * G.Hkv + kvh) * G.nq + (p - (seq_len(G, b) - G.nq)) : cols[h].row;
       int* dst = G.idx + irow * cmax;
       for (long long e = lane; e < cmax; e += 32) {
         long long v = -1;
@@ -734,8 +776,8 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
         if (e <= t) return topj[e - 1];
         return wlo + (e - 1 - t);
       };
-      warp_softmax_pv<BF16, D, NC>(G, kvrow0, qd, h, mEnt, entry, wsm, jsm,
-                                   G.out + cols[h].row * D, lane);
+      warp_softmax_pv<BF16, D, NC>(G, b, kvh, qd, h, mEnt, entry, wsm, jsm, cols[h].row * D,
+                                   lane);
       __syncwarp();
     }
     return;
@@ -752,8 +794,9 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       if (!cols[h].active || i >= tcount[h] || (GROUP && h % G.g != 0)) continue;
       const long long row = topj_all[h * KP + i];
       uint8_t* dst = stage + (size_t)(top0 + sl) * SLOT;
-      bulk_copy_g2s(dst, kb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[2]);
-      bulk_copy_g2s(dst + S::ROWB, vb + (kvrow0 + row) * S::ROWB, S::ROWB, &bars[2]);
+      const long long gr = kv_row(G, b, kvh, row);
+      bulk_copy_g2s(dst, kb + gr * S::ROWB, S::ROWB, &bars[2]);
+      bulk_copy_g2s(dst + S::ROWB, vb + gr * S::ROWB, S::ROWB, &bars[2]);
     }
     const bool ok = mbar_wait(&bars[1], 0) && mbar_wait(&bars[2], 0);
     if (!ok && tid == 0) set_status(G.status, kStatusTimeout);
@@ -831,9 +874,9 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       a1 = fmaf(w[e], v1, a1);
     }
     const float z = zsum[h];
-    float* o = G.out + cols[h].row * D + c;
-    o[0] = z > 0.f ? a0 / z : 0.f;
-    o[1] = z > 0.f ? a1 / z : 0.f;
+    const long long o = cols[h].row * D + c;
+    store_out(G, o, z > 0.f ? a0 / z : 0.f);
+    store_out(G, o + 1, z > 0.f ? a1 / z : 0.f);
   }
 }
 
@@ -1289,7 +1332,6 @@ __global__ void __launch_bounds__(128) sparse_pv_kernel(const Geom G) {
   const int b = (int)(row / (G.nq * G.Hq));
   const int kvh = h / G.g;
   const long long p = G.n - G.nq + r;
-  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
   for (int c = lane; c < D; c += 32) {
     const float x = load_elem<BF16>(G.qp, row * D + c);
     qs[warp][c] = make_float2(x, x);
@@ -1301,8 +1343,8 @@ __global__ void __launch_bounds__(128) sparse_pv_kernel(const Geom G) {
     const int j = irow[e];
     return (j >= 0 && j <= p) ? j : -1;
   };
-  warp_softmax_pv<BF16, D, 1>(G, kvrow0, qs[warp], 0, cmax, entry, wsm[warp], jsm[warp],
-                              G.out + row * D, lane);
+  warp_softmax_pv<BF16, D, 1>(G, b, kvh, qs[warp], 0, cmax, entry, wsm[warp], jsm[warp],
+                              row * D, lane);
 }
 
 // ================================================ condensate KV compaction ==

@@ -849,8 +849,9 @@ __global__ void __launch_bounds__(128) prefill_pv_kernel(const Geom G) {
   };
   const float* qw = qs[warp];
   warp_softmax_pv_with<true, D>(
-      G, kvrow0, [&](long long kr) { return score_row_q4<true, D>(G.kp, kr, qw); }, mEnt, entry,
-      wsm[warp], jsm[warp], G.out + row * D, lane);
+      G, [&](long long j) { return kvrow0 + j; },
+      [&](long long kr) { return score_row_q4<true, D>(G.kp, kr, qw); }, mEnt, entry, wsm[warp],
+      jsm[warp], row * D, lane);
 }
 
 // ------------------------------------------------------- banded softmax ----

@@ -216,14 +216,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int kk = G.topk;
 
   const long long last_col = ((cb + 1) * NC < G.ncols ? (cb + 1) * NC : G.ncols) - 1;
-  const long long pos_max = G.n - G.nq + last_col / G.g;
+  const long long pos_max = seq_len(G, b) - G.nq + last_col / G.g;
   const long long jmax = kk > 0 ? pos_max - G.W : 0;
-  const long long ncand = jmax > 0 ? jmax : 0;
+  // Splits cover keys kbase..jmax: from key 1 (the first candidate), or, for
+  // a paged cache, from key 0 so that every 128-key tile starts on a block
+  // boundary (key 0, the anchor, is then masked out of the candidates).
+  const long long kbase = G.block_table ? 0 : 1;
+  const long long ncand = jmax > 0 ? jmax + 1 - kbase : 0;
   const long long unit = ((long long)b * G.Hkv + kvh) * G.ncb + cb;
   const long long Lu = unit < G.hi_units ? G.L2 : G.L;  // keys per split of this unit
   const int nsplit = ncand > 0 ? (int)((ncand + Lu - 1) / Lu) : 1;
   if (split >= nsplit) return;
-  const long long ks = 1 + (long long)split * Lu;
+  const long long ks = kbase + (long long)split * Lu;
   const long long ke = (ks + Lu - 1 < jmax) ? ks + Lu - 1 : jmax;  // inclusive
   const int ntiles = ke >= ks ? (int)((ke - ks + kTcTile) / kTcTile) : 0;
   const int stages = G.stages;
@@ -277,8 +281,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
 
-  const long long row0 = ((long long)b * G.Hkv + kvh) * G.kv_stride + ks;
-  const long long kvrow0 = ((long long)b * G.Hkv + kvh) * G.kv_stride;
 
   if (warp == 0) {
     // ---------------- TMA producer ------------------------------------------
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         uint8_t* dst = ring + (size_t)s * TILEB;
         mbar_arrive_expect_tx(&full[s], (uint32_t)TILEB);
-        const int y = (int)(row0 + (long long)t * kTcTile);
+        const int y = (int)kv_row(G, b, kvh, ks + (long long)t * kTcTile);
 #pragma unroll
         for (int cc = 0; cc < S::NCH; ++cc)
           tma_load_2d(dst + cc * (kTcTile * 128), &map_k, cc * S::EPC, y, &full[s]);
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int h = 0; h < NC; ++h) {
         if (GROUP && h * gsz >= NC) continue;
-        const bool cand = j <= jh[h];
+        const bool cand = j <= jh[h] && j >= 1;
         bool flag = cand && sc[h] >= thr[h];
         unsigned mask = __ballot_sync(kFull, flag);
         if (mask == 0u) continue;
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // the survivors' K rows on their way to L2 for the exact rescoring
       for (int i = lane; i < kept.keep && i < LL; i += 32)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(
-            reinterpret_cast<const uint8_t*>(G.kp) + (kvrow0 + key_pos(hb[i])) * S::ROWB));
+            reinterpret_cast<const uint8_t*>(G.kp) + kv_row(G, b, kvh, key_pos(hb[i])) * S::ROWB));
     }
   }
   // every role is done with the ring and the accumulators
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         x[ee] = 0ull;
         if (key != 0ull && key_score(key) >= cut) {
           const uint32_t jj = key_pos(key);
-          x[ee] = rank_key(exact_score(kvrow0 + jj, h), jj);
+          x[ee] = rank_key(exact_score(kv_row(G, b, kvh, jj), h), jj);
         }
       }
       warp_sort_desc<LE>(x, lane);
@@ -529,7 +531,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const long long lim = cols[hc].active ? (cols[hc].jhi < ke ? cols[hc].jhi : ke) : 0;
       for (long long j0 = ks; j0 <= lim; j0 += 32) {
         const long long j = j0 + lane;
-        const uint64_t key = j <= lim ? rank_key(exact_score(kvrow0 + j, h), (uint32_t)j) : 0ull;
+        const uint64_t key = (j <= lim && j >= 1)
+                                 ? rank_key(exact_score(kv_row(G, b, kvh, j), h), (uint32_t)j)
+                                 : 0ull;
         offer<FEC, KE>(scratch, fthr, fcnt, key, kk, lane);
       }
       __syncwarp();
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // the V rows the final softmax may gather, on their way to L2
       if (i < kk && cols[hc].active && x[ee] != 0ull && G.vp)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(
-            reinterpret_cast<const uint8_t*>(G.vp) + (kvrow0 + key_pos(x[ee])) * S::ROWB));
+            reinterpret_cast<const uint8_t*>(G.vp) + kv_row(G, b, kvh, key_pos(x[ee])) * S::ROWB));
     }
   }
   if (!finish_split(G.counters + unit, nsplit, misc)) return;

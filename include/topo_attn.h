@@ -78,8 +78,10 @@ enum {
   TOPO_ERR_WORKSPACE = -3,        /* workspace missing, too small or misaligned */
   TOPO_ERR_CUDA = -4,             /* a CUDA runtime/driver call failed at enqueue time */
   TOPO_ERR_DEVICE_TIMEOUT = -5,   /* a bounded device-side wait gave up (see topo_attn_device_status) */
-  TOPO_ERR_SCRATCH_LIMIT = -6     /* topo_attn_forward_noalloc: the problem needs more scratch than
+  TOPO_ERR_SCRATCH_LIMIT = -6,    /* topo_attn_forward_noalloc: the problem needs more scratch than
                                      TOPO_NOALLOC_SCRATCH_BYTES */
+  TOPO_ERR_BAD_BLOCK = -7         /* device status only: a block-table entry of
+                                     topo_attn_forward_paged was outside the pool */
 };
 
 typedef enum { TOPO_F32 = 0, TOPO_BF16 = 1 } topo_dtype;
@@ -142,6 +144,48 @@ int topo_attn_forward(const topo_attn_params *p, const void *q, const void *k, c
 int topo_attn_forward_grouped(const topo_attn_params *p, const void *q, const void *k,
                               const void *v, float *out, int32_t *idx, void *ws,
                               size_t ws_bytes, topo_stream_t stream);
+
+/*
+ * Paged KV cache and output dtype (a serving-shaped boundary for the KV-cache
+ * setting of the pages [zh S4]).
+ *
+ * With block_table != NULL, k_pool and v_pool are pools of fixed-size blocks,
+ *     [num_blocks, Hkv, block_size, d]  (dtype of q),
+ * and key j of sequence b lives in block block_table[b * max_blocks +
+ * j / block_size] at offset j % block_size.  block_size must be a multiple of
+ * 128 (so that every 128-key tile the scorer loads lies in one block) and
+ * max_blocks * block_size >= n.  Entries outside 0..num_blocks-1 are read as
+ * block 0 and reported through the device status word (TOPO_ERR_BAD_BLOCK);
+ * no access leaves the pool.  With block_table == NULL, k_pool and v_pool are
+ * the usual contiguous [B, Hkv, kv_stride, d] caches.
+ * seq_lens (device, optional): the causal length of each sequence (the query
+ * rows sit at positions seq_lens[b] - nq + r), clamped to nq..n; NULL: all n.
+ * out_bf16 != 0: out is bfloat16 [B, Hq, nq, d] (round to nearest even),
+ * else float32.
+ */
+typedef struct {
+  const int32_t *block_table; /* [B, max_blocks] device, or NULL */
+  const int32_t *seq_lens;    /* [B] device, or NULL */
+  int32_t max_blocks;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t out_bf16;
+} topo_paged_kv;
+
+/* Workspace bytes for topo_attn_forward_paged; 0 if invalid or unsupported. */
+size_t topo_attn_paged_workspace_size(const topo_attn_params *p, const topo_paged_kv *kv);
+
+/*
+ * Condensate-set attention (as topo_attn_forward, without the excluded mass)
+ * over a paged or contiguous KV cache with per-sequence lengths and a float32
+ * or bfloat16 output.  p->n is the largest sequence length (p->kv_stride is
+ * read only for a contiguous cache).  Supported on the tensor-core decode
+ * shapes: bf16, nq * Hq/Hkv <= 8 (<= 4 when k > 32), 1 <= k <= 64; otherwise
+ * TOPO_ERR_UNSUPPORTED.  idx (optional) as for topo_attn_forward.
+ */
+int topo_attn_forward_paged(const topo_attn_params *p, const topo_paged_kv *kv, const void *q,
+                            const void *k_pool, const void *v_pool, void *out, int32_t *idx,
+                            void *ws, size_t ws_bytes, topo_stream_t stream);
 
 /* The scoring and selection steps alone [fr S2, ko S3]: writes idx (required). */
 int topo_attn_score_select(const topo_attn_params *p, const void *q, const void *k,

@@ -186,3 +186,26 @@ def test_compact_kv_rejects_bad_arguments(lib):
     assert lib.topo_attn_compact_kv(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE + 4, FAKE, None) == -1
     assert lib.topo_attn_compact_kv(ctypes.byref(_p(d=96)), FAKE, FAKE, FAKE, FAKE, FAKE,
                                     None) == -2
+
+
+def test_paged_rejects_bad_arguments(lib):
+    p = _p(n=4096, kv_stride=4096)
+    table = FAKE
+    kv = topo.PagedKV(table, None, 32, 128, 64, 0)
+    assert lib.topo_attn_paged_workspace_size(ctypes.byref(p), ctypes.byref(kv)) > 0
+    for bad in (dict(block_size=100), dict(block_size=64), dict(max_blocks=8),
+                dict(num_blocks=0)):
+        f = dict(block_table=table, seq_lens=None, max_blocks=32, block_size=128, num_blocks=64,
+                 out_bf16=0)
+        f.update(bad)
+        kvb = topo.PagedKV(**f)
+        rc = lib.topo_attn_forward_paged(ctypes.byref(p), ctypes.byref(kvb), FAKE, FAKE, FAKE,
+                                         FAKE, None, FAKE, 1 << 30, None)
+        assert rc == -1, bad
+    # float32 and prefill-sized shapes are not the tensor-core decode shapes
+    for badp in (_p(dtype=0), _p(nq=64)):
+        rc = lib.topo_attn_forward_paged(ctypes.byref(badp), ctypes.byref(kv), FAKE, FAKE, FAKE,
+                                         FAKE, None, FAKE, 1 << 30, None)
+        assert rc == -2
+    assert lib.topo_attn_forward_paged(ctypes.byref(p), None, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                       1 << 30, None) == -1
