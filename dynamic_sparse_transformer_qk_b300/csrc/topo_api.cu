@@ -188,6 +188,9 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false
       int st = (topo::kMaxSmem - fixed) / (tct + 24);
       if (st > 8) st = 8;
       if (st < 2) return TOPO_ERR_UNSUPPORTED;
+      // after the scan the ring holds every column's concatenated survivors
+      if ((long long)st * tct < (long long)P->NC * topo::kTcEpiWarps * topo::tc_cap(P->KE) * 8)
+        return TOPO_ERR_UNSUPPORTED;
       P->stages = st;
       P->smem = topo::TcSmem(tct, st, P->D, P->NC, P->KE).total;
     }

@@ -146,9 +146,13 @@ __device__ __forceinline__ uint64_t rank_key(float s, uint32_t j) {
 
 __device__ __forceinline__ uint32_t key_pos(uint64_t key) { return ~static_cast<uint32_t>(key); }
 
-__device__ __forceinline__ float key_score(uint64_t key) {
-  const uint32_t o = static_cast<uint32_t>(key >> 32);
+// inverse of ord_score
+__device__ __forceinline__ float ord_to_float(uint32_t o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+__device__ __forceinline__ float key_score(uint64_t key) {
+  return ord_to_float(static_cast<uint32_t>(key >> 32));
 }
 
 // ------------------------------------------------- warp bitonic networks ----
@@ -266,6 +270,12 @@ __device__ __forceinline__ uint64_t warp_list_get(const uint64_t (&x)[E], int i)
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
   return v;
 }
 

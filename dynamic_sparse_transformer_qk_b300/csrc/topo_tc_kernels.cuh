@@ -75,7 +75,7 @@ struct TcSmem {
     o = (o + 15) & ~15;
     qd = o;     o += D * NC * 8;                   // {q, q} float pairs, [c][col]
     buf = o;    o += kTcEpiWarps * NC * tc_cap(KE) * 8;
-    wmeta = o;  o += kTcEpiWarps * NC * 8;         // per warp and column: delta*, overflow
+    wmeta = o;  o += kTcEpiWarps * NC * 16;        // per warp and column: TcMeta
     cols = o;   o += NC * (int)sizeof(ColInfo);
     misc = o;   o += 64;
     total = o + 1024;
@@ -85,44 +85,87 @@ struct TcSmem {
 struct TcMeta {
   float delta;
   int overflow;
+  int count;  // entries left in the buffer after the final cut
+  int pad;
 };
 
 // ------------------------------------------------ approximate-key buffer ----
 //
-// A warp's candidate buffer of keys rank_key(t, j) (t: tensor-core score).
-// Sort it, and keep (as a sorted prefix) the entries with t >= T - 2 delta,
-// T the k-th best t; fewer than k entries: keep all (T = -inf).  Returns the
-// kept count and T.
+// A warp's candidate buffer holds keys rank_key(t, j) (t: tensor-core score),
+// in no particular order.
+
 struct TcKept {
   int keep;
   float T;
 };
 
+// Rounds of the k-th-best search: each round counts the entries at or above
+// three thresholds that split [lo, hi] into quarters (the three warp
+// reductions are independent), so T ends within (max - min) / 4^rounds below
+// the k-th best: a slightly lower cut, which only keeps a few more entries.
+constexpr int kTcRounds = 5;
+
+// Largest of lo and the quarter points tried, with at least k of the values
+// at or above it; count(lo) >= k must hold, count(t) is warp-uniform.
+template <typename F>
+__device__ __forceinline__ float tc_search(float lo, float hi, int k, F count3) {
+#pragma unroll 1
+  for (int r = 0; r < kTcRounds && lo < hi; ++r) {
+    const float q = 0.25f * (hi - lo);
+    const float t1 = lo + q, t2 = lo + 2.f * q, t3 = lo + 3.f * q;
+    int c1, c2, c3;
+    count3(t1, t2, t3, c1, c2, c3);
+    if (c3 >= k) lo = t3;
+    else if (c2 >= k) { lo = t2; hi = t3; }
+    else if (c1 >= k) { lo = t1; hi = t2; }
+    else hi = t1;
+  }
+  return lo;
+}
+
+// Cut a warp's candidate buffer (cnt entries, any order) without sorting it:
+// T is a lower bound of its k-th best tensor-core score (at least k entries
+// score >= T), and the entries with t >= T - 2 delta move, in their order, to
+// the front.  Fewer than k entries: unchanged, T = -inf.
 template <int EC>
-__device__ __noinline__ TcKept tc_compact(uint64_t* buf, int cnt, int k, float two_delta,
-                                          int lane) {
+__device__ __noinline__ TcKept tc_cut(uint64_t* buf, int cnt, int k, float two_delta, int lane) {
   __syncwarp();
+  if (k <= 0 || cnt < k) return TcKept{cnt, -INFINITY};
   uint64_t x[EC];
+  float v[EC];
+  float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int i = e * 32 + lane;
     x[e] = i < cnt ? buf[i] : 0ull;
+    v[e] = i < cnt ? key_score(x[e]) : -INFINITY;
+    mn = i < cnt ? fminf(mn, v[e]) : mn;
+    mx = fmaxf(mx, v[e]);
   }
-  warp_sort_desc<EC>(x, lane);
-  float T = -INFINITY;
-  if (cnt >= k && k > 0) T = key_score(warp_list_get<EC>(x, k - 1));
+  mn = warp_min(mn);
+  mx = warp_max(mx);
+  const float T = tc_search(mn, mx, k, [&](float t1, float t2, float t3, int& c1, int& c2,
+                                            int& c3) {
+    int a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+    for (int e = 0; e < EC; ++e) {
+      a1 += v[e] >= t1 ? 1 : 0;
+      a2 += v[e] >= t2 ? 1 : 0;
+      a3 += v[e] >= t3 ? 1 : 0;
+    }
+    c1 = __reduce_add_sync(kFull, a1);
+    c2 = __reduce_add_sync(kFull, a2);
+    c3 = __reduce_add_sync(kFull, a3);
+  });
   const float cut = T - two_delta;
+  __syncwarp();
   int keep = 0;
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
-    const bool kp = x[e] != 0ull && (T == -INFINITY || key_score(x[e]) >= cut);
-    keep += __popc(__ballot_sync(kFull, kp));
-  }
-  __syncwarp();
-#pragma unroll
-  for (int e = 0; e < EC; ++e) {
-    const int i = e * 32 + lane;
-    buf[i] = i < keep ? x[e] : 0ull;
+    const bool kp = v[e] >= cut;
+    const unsigned m = __ballot_sync(kFull, kp);
+    if (kp) buf[keep + __popc(m & ((1u << lane) - 1u))] = x[e];
+    keep += __popc(m);
   }
   __syncwarp();
   return TcKept{keep, T};
@@ -426,7 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (mask == 0u) continue;
         uint64_t* hb = mybuf + h * CAP;
         if (cnt[h] + __popc(mask) > CAP) {
-          const TcKept kept = tc_compact<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
+          const TcKept kept = tc_cut<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
           cnt[h] = kept.keep;
           T[h] = kept.T;
           thr[h] = T[h] - 2.f * coef[h] * kmag;
@@ -442,25 +485,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cnt[h] += __popc(mask);
       }
     }
-    // final compaction: each buffer keeps its sorted survivors at [0, LL)
+    // final cut: each buffer keeps its survivors (any order) at [0, count)
 #pragma unroll 1
     for (int h = 0; h < (GROUP ? NC / gsz : NC); ++h) {
       uint64_t* hb = mybuf + h * CAP;
-      // A buffer of at most 64 entries sorts in half the network; that
-      // rewrites (and zero-fills) only slots 0..63, so it is used only when
-      // the survivor list read below is 64 entries long (LL == 64).
-      TcKept kept;
-      if (LL == 64 && cnt[h] <= 64)
-        kept = tc_compact<2>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
-      else
-        kept = tc_compact<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
-      if (kept.keep > LL) ovf[h] = true;
+      const TcKept kept = tc_cut<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
       if (lane == 0) {
         meta[e * NC + h].delta = coef[h] * kmag;
         meta[e * NC + h].overflow = ovf[h] ? 1 : 0;
+        meta[e * NC + h].count = kept.keep;
       }
       // the survivors' K rows on their way to L2 for the exact rescoring
-      for (int i = lane; i < kept.keep && i < LL; i += 32)
+      for (int i = lane; i < kept.keep; i += 32)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(
             reinterpret_cast<const uint8_t*>(G.kp) + kv_row(G, b, kvh, key_pos(hb[i])) * S::ROWB));
     }
@@ -488,35 +524,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   };
   for (int h = warp - 2; h >= 0 && h < nsel; h += kTcEpiWarps) {
-    uint64_t a[LE];
-#pragma unroll
-    for (int ee = 0; ee < LE; ++ee) a[ee] = wbuf[(size_t)h * CAP + ee * 32 + lane];
-    float dmax = meta[h].delta;
-    int ov = meta[h].overflow;
-    for (int w = 1; w < kTcEpiWarps; ++w) {
-      uint64_t bb[LE];
+    // the warps' survivors of this column, concatenated in the (now idle) ring
+    uint64_t* cat = reinterpret_cast<uint64_t*>(ring) + (size_t)h * kTcEpiWarps * CAP;
+    float dmax = 0.f;
+    int ov = 0, total = 0;
+    for (int w = 0; w < kTcEpiWarps; ++w) {
+      const TcMeta mt = meta[w * NC + h];
+      dmax = fmaxf(dmax, mt.delta);
+      ov |= mt.overflow;
       const uint64_t* src = wbuf + ((size_t)w * NC + h) * CAP;
-#pragma unroll
-      for (int ee = 0; ee < LE; ++ee) bb[ee] = src[ee * 32 + lane];
-      warp_merge_desc<LE>(a, bb, lane);
-      dmax = fmaxf(dmax, meta[w * NC + h].delta);
-      ov |= meta[w * NC + h].overflow;
+      for (int i = lane; i < mt.count; i += 32) cat[total + i] = src[i];
+      total += mt.count;
     }
-    // survivors of the union: t >= T - 2 delta*, T its k-th best
-    const float Tu = kk > 0 ? key_score(warp_list_get<LE>(a, kk - 1)) : -INFINITY;
-    const bool haveT = kk > 0 && warp_list_get<LE>(a, kk - 1) != 0ull;
-    const float cut = haveT ? Tu - 2.f * dmax : -INFINITY;
-    const uint64_t lastk = warp_list_get<LE>(a, LL - 1);
-    if (lastk != 0ull && key_score(lastk) >= cut) ov = 1;  // more near ties than slots
-    uint64_t* scratch = wbuf + (size_t)h * CAP;  // this column's warp-0 buffer is free now
+    __syncwarp();
+    // survivors of the union: t >= T - 2 delta*, T a lower bound of its k-th
+    // best; none are cut while the union holds fewer than k entries
+    float cut = -INFINITY;
+    if (kk > 0 && total >= kk) {
+      float mn = INFINITY, mx = -INFINITY;
+      for (int i = lane; i < total; i += 32) {
+        const float t = key_score(cat[i]);
+        mn = fminf(mn, t);
+        mx = fmaxf(mx, t);
+      }
+      mn = warp_min(mn);
+      mx = warp_max(mx);
+      const float T = tc_search(mn, mx, kk, [&](float t1, float t2, float t3, int& c1, int& c2,
+                                                 int& c3) {
+        int a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll 4
+        for (int i = lane; i < total; i += 32) {
+          const float t = key_score(cat[i]);
+          a1 += t >= t1 ? 1 : 0;
+          a2 += t >= t2 ? 1 : 0;
+          a3 += t >= t3 ? 1 : 0;
+        }
+        c1 = __reduce_add_sync(kFull, a1);
+        c2 = __reduce_add_sync(kFull, a2);
+        c3 = __reduce_add_sync(kFull, a3);
+      });
+      cut = T - 2.f * dmax;
+    }
+    // move them to the front, in place (a write never passes its read)
+    int ns = 0;
+    for (int i0 = 0; i0 < total && !ov; i0 += 32) {
+      const uint64_t key = i0 + lane < total ? cat[i0 + lane] : 0ull;
+      const bool kp = key != 0ull && key_score(key) >= cut;
+      const unsigned m = __ballot_sync(kFull, kp);
+      __syncwarp();
+      if (kp) cat[ns + __popc(m & ((1u << lane) - 1u))] = key;
+      ns += __popc(m);
+      __syncwarp();
+    }
+    uint64_t* scratch = wbuf + (size_t)h * CAP;  // the fallback's buffer
+    if (ns > LL) ov = 1;  // more near ties than slots
     uint64_t x[LE];
     if (!ov) {
       // rescore the survivors with the exact float32 chain
 #pragma unroll
       for (int ee = 0; ee < LE; ++ee) {
-        const uint64_t key = a[ee];
+        const int i = ee * 32 + lane;
+        const uint64_t key = i < ns ? cat[i] : 0ull;
         x[ee] = 0ull;
-        if (key != 0ull && key_score(key) >= cut) {
+        if (key != 0ull) {
           const uint32_t jj = key_pos(key);
           x[ee] = rank_key(exact_score(kv_row(G, b, kvh, jj), h), jj);
         }
