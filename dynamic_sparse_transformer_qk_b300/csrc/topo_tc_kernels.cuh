@@ -85,7 +85,7 @@ struct TcSmem {
 struct TcMeta {
   float delta;
   int overflow;
-  int count;  // entries left in the buffer after the final cut
+  int count;  // entries in the buffer at the end of the scan
   int pad;
 };
 
@@ -485,21 +485,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cnt[h] += __popc(mask);
       }
     }
-    // final cut: each buffer keeps its survivors (any order) at [0, count)
+    // the buffers go to the per-column stage as they are
 #pragma unroll 1
-    for (int h = 0; h < (GROUP ? NC / gsz : NC); ++h) {
-      uint64_t* hb = mybuf + h * CAP;
-      const TcKept kept = tc_cut<EC>(hb, cnt[h], kk, 2.f * coef[h] * kmag, lane);
+    for (int h = 0; h < (GROUP ? NC / gsz : NC); ++h)
       if (lane == 0) {
         meta[e * NC + h].delta = coef[h] * kmag;
         meta[e * NC + h].overflow = ovf[h] ? 1 : 0;
-        meta[e * NC + h].count = kept.keep;
+        meta[e * NC + h].count = cnt[h];
       }
-      // the survivors' K rows on their way to L2 for the exact rescoring
-      for (int i = lane; i < kept.keep; i += 32)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(
-            reinterpret_cast<const uint8_t*>(G.kp) + kv_row(G, b, kvh, key_pos(hb[i])) * S::ROWB));
-    }
   }
   // every role is done with the ring and the accumulators
   tc::fence_before_sync();
@@ -523,9 +516,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return score_row_global<true, D, NC>(G.kp, row, qd, h);
     }
   };
-  for (int h = warp - 2; h >= 0 && h < nsel; h += kTcEpiWarps) {
-    // the warps' survivors of this column, concatenated in the (now idle) ring
-    uint64_t* cat = reinterpret_cast<uint64_t*>(ring) + (size_t)h * kTcEpiWarps * CAP;
+  // Per selection column: the warps' buffers concatenated in the (now idle)
+  // ring, cut at T - 2 delta* (T a lower bound of the union's k-th best), the
+  // survivors gathered at the front.  Returns the overflow flag (more near
+  // ties than LL slots, or a warp's buffer overflowed).
+  auto gather = [&](int h, uint64_t* cat, int& ns) -> int {
     float dmax = 0.f;
     int ov = 0, total = 0;
     for (int w = 0; w < kTcEpiWarps; ++w) {
@@ -537,8 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       total += mt.count;
     }
     __syncwarp();
-    // survivors of the union: t >= T - 2 delta*, T a lower bound of its k-th
-    // best; none are cut while the union holds fewer than k entries
+    // none are cut while the union holds fewer than k entries
     float cut = -INFINITY;
     if (kk > 0 && total >= kk) {
       float mn = INFINITY, mx = -INFINITY;
@@ -565,8 +559,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       });
       cut = T - 2.f * dmax;
     }
-    // move them to the front, in place (a write never passes its read)
-    int ns = 0;
+    // in place: a write never passes its read
+    ns = 0;
     for (int i0 = 0; i0 < total && !ov; i0 += 32) {
       const uint64_t key = i0 + lane < total ? cat[i0 + lane] : 0ull;
       const bool kp = key != 0ull && key_score(key) >= cut;
@@ -576,21 +570,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ns += __popc(m);
       __syncwarp();
     }
+    return (ov || ns > LL) ? 1 : 0;
+  };
+  // rescore gathered entry i (< ns) with the exact float32 chain
+  auto rescore = [&](int h, const uint64_t* cat, int ns, int i) -> uint64_t {
+    const uint64_t key = i < ns ? cat[i] : 0ull;
+    if (key == 0ull) return 0ull;
+    const uint32_t jj = key_pos(key);
+    return rank_key(exact_score(kv_row(G, b, kvh, jj), h), jj);
+  };
+  // sort the rescored keys (or score the split on the CUDA cores after an
+  // overflow) and publish the split's exact top-k of column h
+  auto publish = [&](int h, uint64_t (&x)[LE], int ov) {
     uint64_t* scratch = wbuf + (size_t)h * CAP;  // the fallback's buffer
-    if (ns > LL) ov = 1;  // more near ties than slots
-    uint64_t x[LE];
     if (!ov) {
-      // rescore the survivors with the exact float32 chain
-#pragma unroll
-      for (int ee = 0; ee < LE; ++ee) {
-        const int i = ee * 32 + lane;
-        const uint64_t key = i < ns ? cat[i] : 0ull;
-        x[ee] = 0ull;
-        if (key != 0ull) {
-          const uint32_t jj = key_pos(key);
-          x[ee] = rank_key(exact_score(kv_row(G, b, kvh, jj), h), jj);
-        }
-      }
       warp_sort_desc<LE>(x, lane);
     } else {
       // fallback: every key of the split through the exact chain (CUDA cores)
@@ -627,6 +620,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (i < kk && cols[hc].active && x[ee] != 0ull && G.vp)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(
             reinterpret_cast<const uint8_t*>(G.vp) + kv_row(G, b, kvh, key_pos(x[ee])) * S::ROWB));
+    }
+  };
+  const int ew = warp - 2;  // epilogue warp, or < 0
+  if (ew >= 0 && 2 * nsel <= kTcEpiWarps) {
+    // two warps per column: the leader gathers, both rescore alternate
+    // 32-entry blocks (into slots LL..2LL of the ring area), the leader sorts
+    // and publishes; a named barrier per column pairs them
+    constexpr int HALF = kTcEpiWarps / 2;
+    const int h = ew % HALF, role = ew / HALF;
+    if (h < nsel) {
+      uint64_t* cat = reinterpret_cast<uint64_t*>(ring) + (size_t)h * kTcEpiWarps * CAP;
+      if (role == 0) {
+        int ns = 0;
+        const int ov = gather(h, cat, ns);
+        if (lane == 0) cat[2 * LL] = (uint64_t)(uint32_t)ns | ((uint64_t)ov << 32);
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + h) : "memory");
+      const uint64_t info = cat[2 * LL];
+      const int ns = (int)(uint32_t)info, ov = (int)(info >> 32);
+      if (!ov) {
+#pragma unroll
+        for (int ee = 0; ee < LE; ++ee)
+          if ((ee & 1) == role) cat[LL + ee * 32 + lane] = rescore(h, cat, ns, ee * 32 + lane);
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + h) : "memory");
+      if (role == 0) {
+        uint64_t x[LE];
+#pragma unroll
+        for (int ee = 0; ee < LE; ++ee) x[ee] = ov ? 0ull : cat[LL + ee * 32 + lane];
+        publish(h, x, ov);
+      }
+    }
+  } else {
+    for (int h = ew; h >= 0 && h < nsel; h += kTcEpiWarps) {
+      uint64_t* cat = reinterpret_cast<uint64_t*>(ring) + (size_t)h * kTcEpiWarps * CAP;
+      int ns = 0;
+      const int ov = gather(h, cat, ns);
+      uint64_t x[LE];
+#pragma unroll
+      for (int ee = 0; ee < LE; ++ee) x[ee] = ov ? 0ull : rescore(h, cat, ns, ee * 32 + lane);
+      publish(h, x, ov);
     }
   }
   if (!finish_split(G.counters + unit, nsplit, misc)) return;
