@@ -27,6 +27,7 @@ struct Plan {
   bool bf16 = false;
   bool tc = false;  // tensor-core select kernel (bf16, <= 8 columns per KV head, 1 <= k <= 64)
   bool pf = false;  // tensor-core chunked-prefill path (bf16, > 8 columns per KV head, k <= 32)
+  bool dtc = false;  // tensor-core dense kernel (bf16, <= 8 columns per KV head)
   int pf_stages = 0, pf_smem = 0, pf_items_per_head = 0, pf_grid = 0, pf_kmax_grid = 1;
   long long pf_nitems = 0;
   int D = 0, NC = 1, KE = 1, KP = 32;
@@ -216,13 +217,26 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false
     const topo::Smem base_e(0, 0, P->D, P->NC, topo::kWarps * P->NC * 16);
     ring_shape(tileb + 16, base_e.total, 32768, &P->stages_e, &P->ncw_e);
     P->smem_e = topo::Smem(tileb, P->stages_e, P->D, P->NC, topo::kWarps * P->NC * 16).total;
-  } else {
-    P->L = choose_split(P->units, pos_max + 1, slots);
+  } else if (P->bf16 && P->ncols <= 8) {
+    // tensor-core dense kernel: all columns of a KV head in one block
+    const int stageb = 2 * topo::kTcTile * P->D * 2;
+    const int fixed = topo::DenseTcSmem(stageb, 0, P->D, P->NC).total;
+    int st = (topo::kMaxSmem - fixed) / (stageb + 24);
+    if (st > 8) st = 8;
+    if (st < 2 || (long long)st * stageb < (long long)topo::kTcEpiWarps * P->NC * (P->D + 2) * 4)
+      return TOPO_ERR_UNSUPPORTED;
+    P->dtc = true;
+    P->stages = st;
+    P->smem = topo::DenseTcSmem(stageb, st, P->D, P->NC).total;
+    P->L = choose_split(P->units, pos_max + 1, slots, topo::kTcTile);
     P->nsplit = (int)ceil_div(pos_max + 1, P->L);
+  } else {
     const int pbuf = topo::kConsumerWarps * kTile * P->NC * 4;
     const topo::Smem base(0, 0, P->D, P->NC, pbuf);
     const int red = topo::kConsumerWarps * P->NC * (P->D + 2) * 4;
     ring_shape(2 * tileb + 16, base.total, red > 32768 ? red : 32768, &P->stages, &P->ncw);
+    P->L = choose_split(P->units, pos_max + 1, slots);
+    P->nsplit = (int)ceil_div(pos_max + 1, P->L);
     P->smem = topo::Smem(2 * tileb, P->stages, P->D, P->NC, pbuf).total;
   }
   if (P->smem > topo::kMaxSmem || P->smem_e > topo::kMaxSmem) return TOPO_ERR_UNSUPPORTED;
@@ -604,8 +618,9 @@ int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, 
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < P.total)
     return TOPO_ERR_WORKSPACE;
   CUtensorMap mk, mv;
-  rc = make_map(&mk, k, p);
-  if (rc == TOPO_OK) rc = make_map(&mv, v, p);
+  const int box = P.dtc ? topo::kTcTile : kTile;
+  rc = make_map(&mk, k, p, box);
+  if (rc == TOPO_OK) rc = make_map(&mv, v, p, box);
   if (rc != TOPO_OK) return rc;
   uint8_t* w = static_cast<uint8_t*>(ws);
   Geom G = base_geom(p, P);
@@ -624,7 +639,10 @@ int dense_attn_forward(const topo_attn_params* p, const void* q, const void* k, 
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = to_status(cudaMemsetAsync(w + P.off_cnt, 0, P.off_part - P.off_cnt, st));
   if (rc != TOPO_OK) return rc;
-  return dispatch(P.bf16, P.D, [&](auto L) { return L.dense(P.NC, mk, mv, G, grid, P.smem, st); });
+  return dispatch(P.bf16, P.D, [&](auto L) {
+    return P.dtc ? L.dense_tc(P.NC, mk, mv, G, grid, P.smem, st)
+                 : L.dense(P.NC, mk, mv, G, grid, P.smem, st);
+  });
 }
 
 int topo_attn_layer_schedule(int32_t L, int32_t pillar_every, const int32_t* windows,

@@ -291,13 +291,14 @@ __device__ __forceinline__ void lane_elems(const uint8_t* p, float (&v)[D / 32])
   }
 }
 
-// Byte offset of this lane's slice of row r inside a swizzled tile.
-template <bool BF16, int D>
+// Byte offset of this lane's slice of row r inside a swizzled tile of ROWS
+// rows (each 128-byte column chunk of the rows stored contiguously).
+template <bool BF16, int D, int ROWS = kTile>
 __device__ __forceinline__ int tile_lane_offset(int r, int lane) {
   using S = Shape<BF16, D>;
   const int byte = lane * S::BPL;
   const int cc = byte >> 7, o = byte & 127;
-  return cc * (kTile * 128) + r * 128 + ((((o >> 4) ^ (r & 7))) << 4) + (o & 15);
+  return cc * (ROWS * 128) + r * 128 + ((((o >> 4) ^ (r & 7))) << 4) + (o & 15);
 }
 
 // ------------------------------------------------------------ pipeline -----
@@ -1189,13 +1190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const long long row0 = ((long long)b * G.Hkv + kvh) * G.kv_stride + ks;
   int issued = 0;
-  float m[NC], l[NC], acc[NC][EPL];
+  static_assert(EPL % 2 == 0, "element pairs per lane");
+  // acc[h][i]: this lane's output elements 2i, 2i+1 of column h (paired FMAs)
+  float m[NC], l[NC];
+  float2 acc[NC][EPL / 2];
 #pragma unroll
   for (int h = 0; h < NC; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+    for (int e = 0; e < EPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
   }
   if (warp == kConsumerWarps) {
     if (lane == 0) {
@@ -1232,7 +1236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       }
                       l[h] = l[h] * alpha + warp_sum(pA + pB);
 #pragma unroll
-                      for (int e = 0; e < EPL; ++e) acc[h][e] *= alpha;
+                      for (int e = 0; e < EPL / 2; ++e) {
+                        acc[h][e].x *= alpha;
+                        acc[h][e].y *= alpha;
+                      }
                       m[h] = mnew;
                       pbuf[lane * NC + h] = pA;
                       pbuf[(lane + 32) * NC + h] = pB;
@@ -1244,12 +1251,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int r = 0; r < nrows; ++r) {
                       float v[EPL];
                       lane_elems<BF16, D>(vt + tile_lane_offset<BF16, D>(r, lane), v);
+                      float pr[NC];
+                      if constexpr (NC % 4 == 0) {
 #pragma unroll
-                      for (int h = 0; h < NC; ++h) {
-                        const float pr = pbuf[r * NC + h];
+                        for (int h = 0; h < NC; h += 4) {
+                          const float4 p4 = *reinterpret_cast<const float4*>(pbuf + r * NC + h);
+                          pr[h] = p4.x;
+                          pr[h + 1] = p4.y;
+                          pr[h + 2] = p4.z;
+                          pr[h + 3] = p4.w;
+                        }
+                      } else {
 #pragma unroll
-                        for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pr, v[e], acc[h][e]);
+                        for (int h = 0; h < NC; ++h) pr[h] = pbuf[r * NC + h];
                       }
+#pragma unroll
+                      for (int h = 0; h < NC; ++h)
+#pragma unroll
+                        for (int e = 0; e < EPL / 2; ++e)
+                          acc[h][e] = __ffma2_rn(make_float2(pr[h], pr[h]),
+                                                 make_float2(v[2 * e], v[2 * e + 1]), acc[h][e]);
                     }
                   });
   }
@@ -1265,7 +1286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         r[1] = l[h];
       }
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) r[2 + lane * EPL + e] = acc[h][e];
+      for (int e = 0; e < EPL / 2; ++e) {
+        r[2 + lane * EPL + 2 * e] = acc[h][e].x;
+        r[2 + lane * EPL + 2 * e + 1] = acc[h][e].y;
+      }
     }
   }
   __syncthreads();

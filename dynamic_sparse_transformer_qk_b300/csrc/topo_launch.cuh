@@ -27,6 +27,9 @@ struct Launcher {
   static cudaError_t compact(const Geom& G, void* k_out, void* v_out, cudaStream_t st);
   static cudaError_t select_tc(int NC, int KE, bool group, const CUtensorMap& mk128,
                                const Geom& G, dim3 grid, int smem, cudaStream_t st);
+  // dense attention on the tensor cores (bf16 only)
+  static cudaError_t dense_tc(int NC, const CUtensorMap& mk128, const CUtensorMap& mv128,
+                              const Geom& G, dim3 grid, int smem, cudaStream_t st);
   // chunked prefill on the tensor cores (bf16 only): K scale, scan, finalize, softmax
   static cudaError_t prefill(const CUtensorMap& mk128, const Geom& G, int scan_grid, int scan_smem,
                              int kmax_grid, bool do_pv, cudaStream_t st);
@@ -168,6 +171,33 @@ cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, bool group, const CUten
       case 2: return run_select_tc_ke<D, 2, false>(KE, mk128, G, grid, smem, st);
       case 4: return run_select_tc_ke<D, 4, false>(KE, mk128, G, grid, smem, st);
       case 8: return run_select_tc_ke<D, 8, false>(KE, mk128, G, grid, smem, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+}
+
+template <int D, int NC>
+cudaError_t run_dense_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Geom& G, dim3 grid,
+                         int smem, cudaStream_t st) {
+  constexpr auto kern = &dense_tc_kernel<D, NC>;
+  const cudaError_t e = allow_smem<kern>();
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTcThreads, smem, st>>>(mk, mv, G);
+  return cudaGetLastError();
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::dense_tc(int NC, const CUtensorMap& mk128,
+                                        const CUtensorMap& mv128, const Geom& G, dim3 grid,
+                                        int smem, cudaStream_t st) {
+  if constexpr (!BF16) {
+    return cudaErrorInvalidValue;
+  } else {
+    switch (NC) {
+      case 1: return run_dense_tc<D, 1>(mk128, mv128, G, grid, smem, st);
+      case 2: return run_dense_tc<D, 2>(mk128, mv128, G, grid, smem, st);
+      case 4: return run_dense_tc<D, 4>(mk128, mv128, G, grid, smem, st);
+      case 8: return run_dense_tc<D, 8>(mk128, mv128, G, grid, smem, st);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -668,4 +668,326 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                 stages * TILEB);
 }
 
+// ============================================ tensor-core dense attention ====
+//
+// Dense causal attention over keys 0..p (the pillar layers, and the
+// reference the condensate set is compared with) for bf16 inputs with every
+// query column of a KV head in one block.  Split-n as the CUDA-core dense
+// kernel; per 128-key tile one MMA scores all columns into TMEM exactly as in
+// the select kernel, and eight epilogue warps -- two per TMEM lane quarter,
+// taking alternate tiles -- each keep an online softmax (m, l) per column
+// over the keys they own and a float32 weighted sum of those keys' V rows,
+// read from the same ring stage (K tile, then V tile).  The warps' states
+// merge in shared memory, the splits' in the CTA that finishes last.
+struct DenseTcSmem {
+  int ring, qtile, bars, qd, pbuf, cols, misc, total;
+  __host__ __device__ DenseTcSmem(int stage_bytes, int stages, int D, int NC) {
+    int o = 0;
+    ring = o;   o += stages * stage_bytes;      // K tile | V tile (multiples of 1024)
+    qtile = o;  o += kTcN * D * 2;              // bf16 B operand (1024-aligned)
+    bars = o;   o += 3 * stages * 8;            // full, empty, mma_done
+    o = (o + 15) & ~15;
+    qd = o;     o += D * NC * 8;
+    pbuf = o;   o += kTcEpiWarps * 32 * NC * 4;  // per warp: weights of its 32 keys
+    cols = o;   o += NC * (int)sizeof(ColInfo);
+    misc = o;   o += 64;
+    total = o + 1024;
+  }
+};
+
+template <int D, int NC>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    dense_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const Geom G) {
+  using S = Shape<true, D>;
+  constexpr int TILEB = kTcTile * S::ROWB;
+  constexpr int STAGEB = 2 * TILEB;
+  constexpr int KSTEPS = D / 16;
+  constexpr int NL = NC <= 4 ? 4 : 8;
+  constexpr int EPL = S::EPL;
+  constexpr int PART = D + 2;  // m, l, acc[D]
+  static_assert(NC <= 8 && EPL % 2 == 0, "dense tensor-core shape");
+
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int split = (int)blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long pos_max = seq_len(G, b) - G.nq + (G.ncols - 1) / G.g;
+  const long long nkeys = pos_max + 1;
+  const int nsplit = (int)((nkeys + G.L - 1) / G.L);
+  if (split >= nsplit) return;
+  const long long ks = (long long)split * G.L;
+  const long long ke = (ks + G.L - 1 < pos_max) ? ks + G.L - 1 : pos_max;
+  const int ntiles = (int)((ke - ks + kTcTile) / kTcTile);
+  const long long unit = (long long)b * G.Hkv + kvh;
+  const int stages = G.stages;
+
+  uint8_t* sm = aligned_smem_base();
+  const DenseTcSmem L(STAGEB, stages, D, NC);
+  uint8_t* ring = sm + L.ring;
+  uint8_t* qtile = sm + L.qtile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* empty = full + stages;
+  uint64_t* mdone = empty + stages;
+  float2* qd = reinterpret_cast<float2*>(sm + L.qd);
+  float* pbuf_all = reinterpret_cast<float*>(sm + L.pbuf);
+  ColInfo* cols = reinterpret_cast<ColInfo*>(sm + L.cols);
+  volatile int* misc = reinterpret_cast<volatile int*>(sm + L.misc);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L.misc + 32);
+
+  if (tid == 0) {
+    misc[0] = 0;  // abort
+    misc[1] = 0;  // last CTA of the unit
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+      mbar_init(&mdone[s], 1);
+    }
+    fence_mbar_init();
+  }
+  load_columns<true, D, NC>(G, b, kvh, 0, cols, qd);
+  __syncthreads();
+  for (int i = tid; i < kTcN * D; i += blockDim.x) {
+    const int r = i / D, c = i % D;
+    const float x = r < NC ? qd[c * NC + r].x : 0.f;
+    *reinterpret_cast<__nv_bfloat16*>(qtile + tc::sw128_offset_bf16(r, c, kTcN)) =
+        __float2bfloat16_rn(x);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  const uint32_t tmem_cols = stages * kTcColsPerStage <= 32
+                                 ? 32u
+                                 : (stages * kTcColsPerStage <= 64
+                                        ? 64u
+                                        : (stages * kTcColsPerStage <= 128 ? 128u : 256u));
+  if (warp == 1) {
+    tc::tmem_alloc(tslot, tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  float m[NC], l[NC];
+  float2 acc[NC][EPL / 2];  // this lane's output elements 2i, 2i+1 (paired FMAs)
+#pragma unroll
+  for (int h = 0; h < NC; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+  }
+
+  if (warp == 0) {
+    // ---------------- TMA producer: K tile, then V tile, per stage ----------
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tmap(&map_k);
+      prefetch_tmap(&map_v);
+      const long long row0 = ((long long)b * G.Hkv + kvh) * G.kv_stride + ks;
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        if (misc[0]) break;
+        const int s = t % stages;
+        const uint32_t round = (uint32_t)(t / stages);
+        if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
+          set_status(G.status, kStatusTimeout);
+          misc[0] = 1;
+          break;
+        }
+        uint8_t* dst = ring + (size_t)s * STAGEB;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)STAGEB);
+        const int y = (int)(row0 + (long long)t * kTcTile);
+#pragma unroll
+        for (int cc = 0; cc < S::NCH; ++cc) {
+          tma_load_2d(dst + cc * (kTcTile * 128), &map_k, cc * S::EPC, y, &full[s]);
+          tma_load_2d(dst + TILEB + cc * (kTcTile * 128), &map_v, cc * S::EPC, y, &full[s]);
+        }
+      }
+      drain_tiles(t, stages, full, G.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer --------------------------------------------
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTcTile, kTcN);
+      const uint32_t qaddr = smem_addr(qtile);
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        if (misc[0]) break;
+        const int s = t % stages;
+        const uint32_t round = (uint32_t)(t / stages);
+        if (!mbar_wait(&empty[s], (round & 1u) ^ 1u) || !mbar_wait(&full[s], round & 1u)) {
+          set_status(G.status, kStatusTimeout);
+          misc[0] = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t aaddr = smem_addr(ring + (size_t)s * STAGEB);
+#pragma unroll
+        for (int ks16 = 0; ks16 < KSTEPS; ++ks16) {
+          const uint32_t ao = aaddr + (ks16 >> 2) * (kTcTile * 128) + (ks16 & 3) * 32;
+          const uint32_t bo = qaddr + (ks16 >> 2) * (kTcN * 128) + (ks16 & 3) * 32;
+          tc::mma_bf16(tmem + (uint32_t)(s * kTcColsPerStage), tc::smem_desc_sw128(ao),
+                       tc::smem_desc_sw128(bo), idesc, ks16 > 0);
+        }
+        tc::mma_commit(&mdone[s]);
+      }
+      if (t > 0) {
+        const int tl = t - 1;
+        if (!mbar_wait(&mdone[tl % stages], (uint32_t)(tl / stages) & 1u))
+          set_status(G.status, kStatusTimeout);
+      }
+    }
+  } else {
+    // ---------------- epilogue: online softmax and weighted sum -------------
+    const int e = warp - 2;           // 0..7
+    const int half = e >> 2;          // tiles t with t % 2 == half
+    const int quarter = warp & 3;     // TMEM lanes (tile rows) 32*quarter .. +31
+    float* pb = pbuf_all + e * 32 * NC;
+    long long lim[NC];
+#pragma unroll
+    for (int h = 0; h < NC; ++h) {
+      const long long p = cols[h].active ? cols[h].pos : -1;
+      lim[h] = p < ke ? p : ke;
+    }
+    for (int t = half; t < ntiles; t += 2) {
+      const int s = t % stages;
+      const uint32_t round = (uint32_t)(t / stages);
+      const bool ok = __all_sync(kFull, mbar_wait(&mdone[s], round & 1u));
+      if (!ok || misc[0]) {
+        if (!ok && lane == 0) {
+          set_status(G.status, kStatusTimeout);
+          misc[0] = 1;
+        }
+        break;
+      }
+      tc::fence_after_sync();
+      float sc[NL];
+      tmem_ld_cols<NL>(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(s * kTcColsPerStage),
+                       sc);
+      tc::tmem_ld_wait();
+      const long long r0 = ks + (long long)t * kTcTile + quarter * 32;  // this warp's first key
+      const long long j = r0 + lane;
+#pragma unroll
+      for (int h = 0; h < NC; ++h) {
+        const float lg = j <= lim[h] ? G.scale * sc[h] : -INFINITY;
+        const float mnew = fmaxf(m[h], warp_max(lg));
+        float p = 0.f, alpha = 1.f;
+        if (mnew != -INFINITY) {
+          alpha = m[h] == -INFINITY ? 0.f : expf(m[h] - mnew);
+          p = lg == -INFINITY ? 0.f : expf(lg - mnew);
+        }
+        l[h] = l[h] * alpha + warp_sum(p);
+#pragma unroll
+        for (int i = 0; i < EPL / 2; ++i) {
+          acc[h][i].x *= alpha;
+          acc[h][i].y *= alpha;
+        }
+        m[h] = mnew;
+        pb[lane * NC + h] = p;
+      }
+      __syncwarp();
+      // rows past the split's last key are skipped (their V may be anything)
+      const int nrows = (int)(ke - r0 + 1 < 32 ? (ke - r0 + 1 > 0 ? ke - r0 + 1 : 0) : 32);
+      const uint8_t* vt = ring + (size_t)s * STAGEB + TILEB;
+#pragma unroll 2
+      for (int rr = 0; rr < nrows; ++rr) {
+        float v[EPL];
+        lane_elems<true, D>(vt + tile_lane_offset<true, D, kTcTile>(quarter * 32 + rr, lane), v);
+        float pr[NC];
+        if constexpr (NC % 4 == 0) {
+#pragma unroll
+          for (int h = 0; h < NC; h += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pb + rr * NC + h);
+            pr[h] = p4.x;
+            pr[h + 1] = p4.y;
+            pr[h + 2] = p4.z;
+            pr[h + 3] = p4.w;
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < NC; ++h) pr[h] = pb[rr * NC + h];
+        }
+#pragma unroll
+        for (int h = 0; h < NC; ++h)
+#pragma unroll
+          for (int i = 0; i < EPL / 2; ++i)
+            acc[h][i] = __ffma2_rn(make_float2(pr[h], pr[h]), make_float2(v[2 * i], v[2 * i + 1]),
+                                   acc[h][i]);
+      }
+      // this warp is done with the stage's accumulator and V rows
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, tmem_cols);
+  }
+  // combine the epilogue warps in shared memory (the ring is free), publish
+  float* red = reinterpret_cast<float*>(ring);  // [epilogue warp][NC][PART]
+  if (warp >= 2) {
+    const int e = warp - 2;
+#pragma unroll
+    for (int h = 0; h < NC; ++h) {
+      float* r = red + ((size_t)e * NC + h) * PART;
+      if (lane == 0) {
+        r[0] = m[h];
+        r[1] = l[h];
+      }
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) {
+        r[2 + lane * EPL + 2 * i] = acc[h][i].x;
+        r[2 + lane * EPL + 2 * i + 1] = acc[h][i].y;
+      }
+    }
+  }
+  __syncthreads();
+  for (int h = warp; h < NC; h += kTcWarps) {
+    float mm = -INFINITY;
+    for (int w = 0; w < kTcEpiWarps; ++w) mm = fmaxf(mm, red[((size_t)w * NC + h) * PART]);
+    float ll = 0.f, o[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) o[i] = 0.f;
+    if (mm != -INFINITY) {
+      for (int w = 0; w < kTcEpiWarps; ++w) {
+        const float* r = red + ((size_t)w * NC + h) * PART;
+        const float f = r[0] == -INFINITY ? 0.f : expf(r[0] - mm);
+        ll += r[1] * f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) o[i] += r[2 + lane * EPL + i] * f;
+      }
+    }
+    float* dst = G.partials + (((size_t)unit * G.nsplit_max + split) * NC + h) * PART;
+    if (lane == 0) {
+      dst[0] = mm;
+      dst[1] = ll;
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) dst[2 + lane * EPL + i] = o[i];
+  }
+  if (!finish_split(G.counters + unit, nsplit, misc)) return;
+  for (int h = warp; h < NC; h += kTcWarps) {
+    if (!cols[h].active) continue;
+    float mm = -INFINITY;
+    for (int s2 = 0; s2 < nsplit; ++s2)
+      mm = fmaxf(mm, __ldcg(G.partials + (((size_t)unit * G.nsplit_max + s2) * NC + h) * PART));
+    float ll = 0.f, o[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) o[i] = 0.f;
+    for (int s2 = 0; s2 < nsplit; ++s2) {
+      const float* r = G.partials + (((size_t)unit * G.nsplit_max + s2) * NC + h) * PART;
+      const float rm = __ldcg(r);
+      const float f = rm == -INFINITY ? 0.f : expf(rm - mm);
+      ll += __ldcg(r + 1) * f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) o[i] += __ldcg(r + 2 + lane * EPL + i) * f;
+    }
+    const long long ob = cols[h].row * D + lane * EPL;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) store_out(G, ob + i, ll > 0.f ? o[i] / ll : 0.f);
+  }
+}
+
 }  // namespace topo

@@ -294,7 +294,15 @@ def test_sparse_softmax_pv_ignores_out_of_range_entries():
 @pytest.mark.parametrize("kw", [dict(), dict(dtype="bf16", d=128, Hq=8, Hkv=2),
                                 dict(n=3000, nq=1, Hq=4, Hkv=1), dict(n=1, nq=1),
                                 dict(d=128, n=32768, nq=1), dict(d=128, n=5000, nq=8),
-                                dict(d=128, n=4000, nq=3, Hq=8, Hkv=2)])
+                                dict(d=128, n=4000, nq=3, Hq=8, Hkv=2),
+                                # bf16 with at most 8 query columns per KV head: the
+                                # tensor-core dense kernel (128-key tiles, ragged tails)
+                                dict(dtype="bf16", d=128, n=5000, nq=1, Hq=32, Hkv=8),
+                                dict(dtype="bf16", d=64, n=3001, nq=2, Hq=8, Hkv=2),
+                                dict(dtype="bf16", d=128, n=130, nq=3, Hq=4, Hkv=2),
+                                dict(dtype="bf16", d=128, n=1, nq=1, Hq=2, Hkv=2),
+                                dict(dtype="bf16", d=128, n=777, nq=1, Hq=2, Hkv=2,
+                                     kv_stride=1000, nan_tail=True)])
 def test_dense_matches_oracle(kw):
     w = W0.with_(n=700, nq=700).with_(**kw)
     x = synth.make(w)
