@@ -134,6 +134,23 @@ void ring_shape(int stage_bytes, int fixed_bytes, int min_ring, int* stages, int
   *ncw = *stages < topo::kConsumerWarps ? *stages : topo::kConsumerWarps;
 }
 
+// Shared memory that select_tail's staged softmax needs for one selection
+// column of gsz columns (its layout: top-k positions and counts, the split
+// lists, logits, the band, anchor and top-k rows, the slot table).  One
+// selection column is one query row, so the band is W rows.
+int tail_scratch_bytes(const topo_attn_params* p, const Plan& P, int gsz) {
+  const long long NC = P.NC, KP = P.KP, kk = p->k;
+  const long long mmax = 1 + (long long)p->W + kk;
+  const long long slot = 2LL * P.D * 2 + 16;
+  const long long v0 = (NC * KP * 4 + NC * 8 + 32 + 1023) & ~1023LL;
+  const long long lists = (long long)P.nsplit * NC * KP * 8;
+  const long long off_lw = (v0 + lists + 1023) & ~1023LL;
+  const long long off_stage = (off_lw + NC * mmax * 4 + NC * 4 + 1023) & ~1023LL;
+  const long long nslots = (long long)p->W + 1 + gsz * kk;
+  const long long need = off_stage + nslots * slot + NC * mmax * 4;
+  return need > (1LL << 30) ? (1 << 30) : (int)need;
+}
+
 // Plan for the condensate-set passes (dense=false) or the dense pass.  A
 // paged cache scans from key 0 (block-aligned tiles), one more key per
 // split range.
@@ -486,9 +503,23 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
     CUtensorMap mk128;
     rc = make_map(&mk128, k, p, topo::kTcTile, pool_rows);
     if (rc != TOPO_OK) return rc;
+    // the tail as a dependent kernel, one CTA per selection column, when its
+    // staged softmax fits in one CTA's shared memory
+    const int gsz = group ? p->Hq / p->Hkv : 1;
+    const int tail_scratch = tail_scratch_bytes(p, P, gsz);
+    const int tail_smem =
+        topo::TailSmem(tail_scratch, P.D, P.NC, P.KP).total;
+    const bool split_tail = tail_smem <= topo::kMaxSmem;
+    if (split_tail) G.flags |= topo::kSplitTail;
     rc = dispatch(P.bf16, P.D, [&](auto L) {
       return L.select_tc(P.NC, P.KE, group, mk128, G, grid, P.smem, st);
     });
+    if (rc == TOPO_OK && split_tail) {
+      const dim3 tgrid((unsigned)(P.ncols / gsz), (unsigned)p->Hkv, (unsigned)p->B);
+      rc = dispatch(P.bf16, P.D, [&](auto L) {
+        return L.tail_tc(P.NC, P.KE, group, G, tgrid, tail_smem, tail_scratch, st);
+      });
+    }
   } else {
     rc = dispatch(P.bf16, P.D,
                   [&](auto L) { return L.select(P.NC, P.KE, mk, G, grid, P.smem, st); });

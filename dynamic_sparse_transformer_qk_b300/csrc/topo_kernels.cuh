@@ -29,7 +29,9 @@
 
 namespace topo {
 
-enum : int { kDoIdx = 1, kDoPV = 2, kSaveThr = 4 };
+// kSplitTail: the tensor-core select kernel only publishes its split lists;
+// a dependent tail kernel merges them (one CTA per selection column).
+enum : int { kDoIdx = 1, kDoPV = 2, kSaveThr = 4, kSplitTail = 8 };
 
 // Everything a kernel needs, passed by value.
 struct Geom {
@@ -580,7 +582,8 @@ __device__ __forceinline__ void warp_softmax_pv(const Geom& G, int b, int kvh, c
 template <bool BF16, int D, int NC, int KE, int NW, bool GROUP = false>
 __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nsplit, int b, int kvh,
                                          const ColInfo* cols, const float2* qd, uint64_t* run,
-                                         uint8_t* scratch, int scratch_bytes) {
+                                         uint8_t* scratch, int scratch_bytes, int h0 = 0,
+                                         int h1 = NC) {
   using S = Shape<BF16, D>;
   constexpr int KP = 32 * KE;
   // a staged slot: the K row, then the V row, then 16 bytes of padding, so
@@ -616,7 +619,8 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   const long long nb = phi - band_lo + 1;
   const long long anchor_slot = band_lo == 0 ? 0 : nb;
   const long long top0 = nb + 1;
-  const long long nslots = top0 + (long long)NC * kk;
+  // top-k slots for columns h0..h1-1 (the columns that may be active)
+  const long long nslots = top0 + (long long)(h1 - h0) * kk;
   const bool fast = (G.flags & kDoPV) && phi >= 0 &&
                     (long long)off_stage + nslots * SLOT + (long long)NC * mmax * 4 <=
                         scratch_bytes;
@@ -794,7 +798,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       const int h = (int)(sl / kk), i = (int)(sl % kk);
       if (!cols[h].active || i >= tcount[h] || (GROUP && h % G.g != 0)) continue;
       const long long row = topj_all[h * KP + i];
-      uint8_t* dst = stage + (size_t)(top0 + sl) * SLOT;
+      uint8_t* dst = stage + (size_t)(top0 + (long long)(h - h0) * kk + i) * SLOT;
       const long long gr = kv_row(G, b, kvh, row);
       bulk_copy_g2s(dst, kb + gr * S::ROWB, S::ROWB, &bars[2]);
       bulk_copy_g2s(dst + S::ROWB, vb + gr * S::ROWB, S::ROWB, &bars[2]);
@@ -826,7 +830,7 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
     long long sl;
     if (p - W + 1 <= 0) sl = e - band_lo;  // 0..p lies in the band, which starts at 0
     else if (e == 0) sl = anchor_slot;
-    else if (e <= t) sl = top0 + (long long)(GROUP ? h - h % G.g : h) * kk + (e - 1);
+    else if (e <= t) sl = top0 + (long long)((GROUP ? h - h % G.g : h) - h0) * kk + (e - 1);
     else sl = (p - W + 1) + (e - 1 - t) - band_lo;
     slot_tab[i] = (int)sl;
     lw[i] = scale * score_row_smem<BF16, D, NC>(stage + (size_t)sl * SLOT, qd, h);

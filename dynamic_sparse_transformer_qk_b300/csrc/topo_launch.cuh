@@ -27,6 +27,9 @@ struct Launcher {
   static cudaError_t compact(const Geom& G, void* k_out, void* v_out, cudaStream_t st);
   static cudaError_t select_tc(int NC, int KE, bool group, const CUtensorMap& mk128,
                                const Geom& G, dim3 grid, int smem, cudaStream_t st);
+  // the tail of a kSplitTail select launch, as its programmatic dependent
+  static cudaError_t tail_tc(int NC, int KE, bool group, const Geom& G, dim3 grid, int smem,
+                             int scratch_bytes, cudaStream_t st);
   // dense attention on the tensor cores (bf16 only)
   static cudaError_t dense_tc(int NC, const CUtensorMap& mk128, const CUtensorMap& mv128,
                               const Geom& G, dim3 grid, int smem, cudaStream_t st);
@@ -171,6 +174,58 @@ cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, bool group, const CUten
       case 2: return run_select_tc_ke<D, 2, false>(KE, mk128, G, grid, smem, st);
       case 4: return run_select_tc_ke<D, 4, false>(KE, mk128, G, grid, smem, st);
       case 8: return run_select_tc_ke<D, 8, false>(KE, mk128, G, grid, smem, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+}
+
+template <int D, int NC, int KE, bool GROUP>
+cudaError_t run_tail_tc(const Geom& G, dim3 grid, int smem, int scratch_bytes, cudaStream_t st) {
+  constexpr auto kern = &topo_tail_tc_kernel<D, NC, KE, GROUP>;
+  const cudaError_t e = allow_smem<kern>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, G, scratch_bytes);
+}
+
+template <int D, int NC, bool GROUP>
+cudaError_t run_tail_tc_ke(int KE, const Geom& G, dim3 grid, int smem, int scratch_bytes,
+                           cudaStream_t st) {
+  if (KE == 1) return run_tail_tc<D, NC, 1, GROUP>(G, grid, smem, scratch_bytes, st);
+  if constexpr (NC <= 4) {
+    if (KE == 2) return run_tail_tc<D, NC, 2, GROUP>(G, grid, smem, scratch_bytes, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <bool BF16, int D>
+cudaError_t Launcher<BF16, D>::tail_tc(int NC, int KE, bool group, const Geom& G, dim3 grid,
+                                       int smem, int scratch_bytes, cudaStream_t st) {
+  if constexpr (!BF16) {
+    return cudaErrorInvalidValue;
+  } else {
+    if (group) {
+      switch (NC) {
+        case 2: return run_tail_tc_ke<D, 2, true>(KE, G, grid, smem, scratch_bytes, st);
+        case 4: return run_tail_tc_ke<D, 4, true>(KE, G, grid, smem, scratch_bytes, st);
+        case 8: return run_tail_tc_ke<D, 8, true>(KE, G, grid, smem, scratch_bytes, st);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+    switch (NC) {
+      case 1: return run_tail_tc_ke<D, 1, false>(KE, G, grid, smem, scratch_bytes, st);
+      case 2: return run_tail_tc_ke<D, 2, false>(KE, G, grid, smem, scratch_bytes, st);
+      case 4: return run_tail_tc_ke<D, 4, false>(KE, G, grid, smem, scratch_bytes, st);
+      case 8: return run_tail_tc_ke<D, 8, false>(KE, G, grid, smem, scratch_bytes, st);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -223,6 +223,29 @@ __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, float (&v)[16])
   tc::tmem_ld16(taddr, v);
 }
 
+// Split geometry of one (sequence, KV head, column block) unit of the
+// tensor-core select kernel: splits cover keys kbase..jmax, from key 1 (the
+// first candidate), or, for a paged cache, from key 0 so that every 128-key
+// tile starts on a block boundary (key 0, the anchor, is then masked out of
+// the candidates).  The tail kernel recomputes it to find the split lists.
+struct TcSplits {
+  long long jmax, kbase, unit, Lu;
+  int nsplit;
+};
+
+__device__ __forceinline__ TcSplits tc_splits(const Geom& G, int b, int kvh, long long cb) {
+  TcSplits r;
+  const long long last_col = G.ncols - 1;  // the tensor-core kernel has one column block
+  const long long pos_max = seq_len(G, b) - G.nq + last_col / G.g;
+  r.jmax = G.topk > 0 ? pos_max - G.W : 0;
+  r.kbase = G.block_table ? 0 : 1;
+  const long long ncand = r.jmax > 0 ? r.jmax + 1 - r.kbase : 0;
+  r.unit = ((long long)b * G.Hkv + kvh) * G.ncb + cb;
+  r.Lu = r.unit < G.hi_units ? G.L2 : G.L;  // keys per split of this unit
+  r.nsplit = ncand > 0 ? (int)((ncand + r.Lu - 1) / r.Lu) : 1;
+  return r;
+}
+
 // ======================================== tensor-core select kernel ==========
 //
 // Grid and workspace as topo_select_kernel (grid.x = column block x split,
@@ -258,17 +281,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kk = G.topk;
 
-  const long long last_col = ((cb + 1) * NC < G.ncols ? (cb + 1) * NC : G.ncols) - 1;
-  const long long pos_max = seq_len(G, b) - G.nq + last_col / G.g;
-  const long long jmax = kk > 0 ? pos_max - G.W : 0;
-  // Splits cover keys kbase..jmax: from key 1 (the first candidate), or, for
-  // a paged cache, from key 0 so that every 128-key tile starts on a block
-  // boundary (key 0, the anchor, is then masked out of the candidates).
-  const long long kbase = G.block_table ? 0 : 1;
-  const long long ncand = jmax > 0 ? jmax + 1 - kbase : 0;
-  const long long unit = ((long long)b * G.Hkv + kvh) * G.ncb + cb;
-  const long long Lu = unit < G.hi_units ? G.L2 : G.L;  // keys per split of this unit
-  const int nsplit = ncand > 0 ? (int)((ncand + Lu - 1) / Lu) : 1;
+  // a dependent tail kernel may start its set-up now (it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const TcSplits sp = tc_splits(G, b, kvh, cb);
+  const long long jmax = sp.jmax, kbase = sp.kbase, unit = sp.unit, Lu = sp.Lu;
+  const int nsplit = sp.nsplit;
   if (split >= nsplit) return;
   const long long ks = kbase + (long long)split * Lu;
   const long long ke = (ks + Lu - 1 < jmax) ? ks + Lu - 1 : jmax;  // inclusive
@@ -663,9 +680,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       publish(h, x, ov);
     }
   }
+  if (G.flags & kSplitTail) return;  // the tail kernel takes it from here
   if (!finish_split(G.counters + unit, nsplit, misc)) return;
   select_tail<true, D, NC, KE, kTcWarps, GROUP>(G, unit, nsplit, b, kvh, cols, qd, wbuf, ring,
                                                 stages * TILEB);
+}
+
+// ============================================== tensor-core select: tail ====
+//
+// With kSplitTail the select kernel stops after publishing its split lists
+// and this kernel, launched as its programmatic dependent, does the tail one
+// selection column per CTA (grid.x: columns, or rows of group-shared sets):
+// merge the splits' lists, write C_i, stage the set's K and V rows and take
+// the softmax (select_tail restricted to the CTA's columns).  Its set-up
+// overlaps the end of the scan; the lists are read only after the wait on
+// the select grid, whose completion makes them visible.
+struct TailSmem {
+  int run, cols, qd, misc, total;
+  __host__ __device__ TailSmem(int scratch_bytes, int D, int NC, int KP) {
+    int o = (scratch_bytes + 1023) & ~1023;  // select_tail's scratch first
+    run = o;   o += NC * KP * 8;
+    cols = o;  o += NC * (int)sizeof(ColInfo);
+    qd = o;    o += D * NC * 8;
+    misc = o;  o += 64;
+    total = o + 1024;
+  }
+};
+
+template <int D, int NC, int KE, bool GROUP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    topo_tail_tc_kernel(const Geom G, int scratch_bytes) {
+  constexpr int KP = 32 * KE;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int gsz = GROUP ? G.g : 1;
+  const int h0 = (int)blockIdx.x * gsz, h1 = h0 + gsz;
+  uint8_t* sm = aligned_smem_base();
+  const TailSmem L(scratch_bytes, D, NC, KP);
+  uint64_t* run = reinterpret_cast<uint64_t*>(sm + L.run);
+  ColInfo* cols = reinterpret_cast<ColInfo*>(sm + L.cols);
+  float2* qd = reinterpret_cast<float2*>(sm + L.qd);
+  load_columns<true, D, NC>(G, b, kvh, 0, cols, qd);
+  __syncthreads();
+  if (threadIdx.x < NC && ((int)threadIdx.x < h0 || (int)threadIdx.x >= h1))
+    cols[threadIdx.x].active = 0;
+  const TcSplits sp = tc_splits(G, b, kvh, 0);
+  // the select grid has completed and its lists are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  select_tail<true, D, NC, KE, kTcWarps, GROUP>(G, sp.unit, sp.nsplit, b, kvh, cols, qd, run, sm,
+                                                scratch_bytes, h0, h1);
 }
 
 // ============================================ tensor-core dense attention ====
