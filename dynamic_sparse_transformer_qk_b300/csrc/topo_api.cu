@@ -38,6 +38,10 @@ struct Plan {
   // excluded-mass pass
   long long Le = kTile;
   int nsplit_e = 1, stages_e = 2, ncw_e = 2, smem_e = 0;
+  // its column blocks: the select pass's, except that 16 tensor-core columns
+  // are two blocks of 8 (the saved k-th keys keep the layout unit * NC + h)
+  int NCe = 1;
+  long long ncbe = 1, units_e = 0;
   // workspace layout (bytes)
   size_t off_cnt = 0, off_cnt_e = 0, off_kmax = 0, off_work = 0, off_zero_end = 0;
   size_t off_lists = 0, off_thr = 0, off_part = 0, off_surv = 0, off_scnt = 0, off_topk = 0;
@@ -171,7 +175,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false
   const int slots = sm_count();
   const long long pos_max = p->n - 1;
   P->tc = !dense && P->bf16 && p->k >= 1 &&
-          ((p->k <= 32 && P->ncols <= 8) || (p->k <= 64 && P->ncols <= 4));
+          ((p->k <= 32 && P->ncols <= 16) || (p->k <= 64 && P->ncols <= 4));
   P->pf = !dense && P->bf16 && !P->tc && p->k >= 1 && p->k <= 32 && P->ncols > 8;
   if (P->tc) {
     // tensor-core scorer: all columns of a KV head in one block
@@ -207,7 +211,9 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false
       if (st > 8) st = 8;
       if (st < 2) return TOPO_ERR_UNSUPPORTED;
       // after the scan the ring holds every column's concatenated survivors
-      if ((long long)st * tct < (long long)P->NC * topo::kTcEpiWarps * topo::tc_cap(P->KE) * 8)
+      // (one area per column with at most four columns, else one per epilogue warp)
+      const long long areas = P->NC < topo::kTcEpiWarps ? P->NC : topo::kTcEpiWarps;
+      if ((long long)st * tct < areas * topo::kTcEpiWarps * topo::tc_cap(P->KE) * 8)
         return TOPO_ERR_UNSUPPORTED;
       P->stages = st;
       P->smem = topo::TcSmem(tct, st, P->D, P->NC, P->KE).total;
@@ -229,11 +235,14 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false
       if (P->pf_smem > topo::kMaxSmem) return TOPO_ERR_UNSUPPORTED;
     }
     // excluded-mass pass: keys 0..p
-    P->Le = choose_split(P->units, pos_max + 1, slots);
+    P->NCe = P->NC > 8 ? 8 : P->NC;
+    P->ncbe = P->NC > 8 ? ceil_div(P->ncols, 8) : P->ncb;
+    P->units_e = (long long)p->B * p->Hkv * P->ncbe;
+    P->Le = choose_split(P->units_e, pos_max + 1, slots);
     P->nsplit_e = (int)ceil_div(pos_max + 1, P->Le);
-    const topo::Smem base_e(0, 0, P->D, P->NC, topo::kWarps * P->NC * 16);
+    const topo::Smem base_e(0, 0, P->D, P->NCe, topo::kWarps * P->NCe * 16);
     ring_shape(tileb + 16, base_e.total, 32768, &P->stages_e, &P->ncw_e);
-    P->smem_e = topo::Smem(tileb, P->stages_e, P->D, P->NC, topo::kWarps * P->NC * 16).total;
+    P->smem_e = topo::Smem(tileb, P->stages_e, P->D, P->NCe, topo::kWarps * P->NCe * 16).total;
   } else if (P->bf16 && P->ncols <= 8) {
     // tensor-core dense kernel: all columns of a KV head in one block
     const int stageb = 2 * topo::kTcTile * P->D * 2;
@@ -257,14 +266,14 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false
     P->smem = topo::Smem(2 * tileb, P->stages, P->D, P->NC, pbuf).total;
   }
   if (P->smem > topo::kMaxSmem || P->smem_e > topo::kMaxSmem) return TOPO_ERR_UNSUPPORTED;
-  if (P->ncb * P->nsplit > 0x7fffffffLL || P->ncb * P->nsplit_e > 0x7fffffffLL)
+  if (P->ncb * P->nsplit > 0x7fffffffLL || P->ncbe * P->nsplit_e > 0x7fffffffLL)
     return TOPO_ERR_UNSUPPORTED;
   // workspace: status word, counters, then per-pass buffers
   size_t o = 256;
   P->off_cnt = o;
   o = align256(o + (size_t)P->units * 4);
   P->off_cnt_e = o;
-  o = align256(o + (size_t)P->units * 4);
+  o = align256(o + (size_t)(P->units_e > P->units ? P->units_e : P->units) * 4);
   P->off_kmax = o;
   o = align256(o + (size_t)p->B * p->Hkv * 4);
   P->off_work = o;
@@ -276,7 +285,7 @@ int make_plan(const topo_attn_params* p, bool dense, Plan* P, bool paged = false
     P->off_thr = o;
     o = align256(o + (size_t)P->units * P->NC * 8);
     P->off_part = o;
-    o = align256(o + (size_t)P->units * P->nsplit_e * P->NC * 16);
+    o = align256(o + (size_t)P->units_e * P->nsplit_e * P->NCe * 16);
     if (P->pf) {
       const size_t ncolumns = (size_t)p->B * p->Hkv * P->ncols;
       P->off_surv = o;
@@ -531,8 +540,9 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
   E.nsplit_max = P.nsplit_e;
   E.stages = P.stages_e;
   E.ncw = P.ncw_e;
-  const dim3 grid_e((unsigned)(P.ncb * P.nsplit_e), (unsigned)p->Hkv, (unsigned)p->B);
-  return dispatch(P.bf16, P.D, [&](auto L) { return L.excl(P.NC, mk, E, grid_e, P.smem_e, st); });
+  E.ncb = P.ncbe;
+  const dim3 grid_e((unsigned)(P.ncbe * P.nsplit_e), (unsigned)p->Hkv, (unsigned)p->B);
+  return dispatch(P.bf16, P.D, [&](auto L) { return L.excl(P.NCe, mk, E, grid_e, P.smem_e, st); });
 }
 
 }  // namespace

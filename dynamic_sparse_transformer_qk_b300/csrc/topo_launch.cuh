@@ -166,6 +166,7 @@ cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, bool group, const CUten
         case 2: return run_select_tc_ke<D, 2, true>(KE, mk128, G, grid, smem, st);
         case 4: return run_select_tc_ke<D, 4, true>(KE, mk128, G, grid, smem, st);
         case 8: return run_select_tc_ke<D, 8, true>(KE, mk128, G, grid, smem, st);
+        case 16: return run_select_tc_ke<D, 16, true>(KE, mk128, G, grid, smem, st);
         default: return cudaErrorInvalidValue;
       }
     }
@@ -174,6 +175,7 @@ cudaError_t Launcher<BF16, D>::select_tc(int NC, int KE, bool group, const CUten
       case 2: return run_select_tc_ke<D, 2, false>(KE, mk128, G, grid, smem, st);
       case 4: return run_select_tc_ke<D, 4, false>(KE, mk128, G, grid, smem, st);
       case 8: return run_select_tc_ke<D, 8, false>(KE, mk128, G, grid, smem, st);
+      case 16: return run_select_tc_ke<D, 16, false>(KE, mk128, G, grid, smem, st);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -218,6 +220,7 @@ cudaError_t Launcher<BF16, D>::tail_tc(int NC, int KE, bool group, const Geom& G
         case 2: return run_tail_tc_ke<D, 2, true>(KE, G, grid, smem, scratch_bytes, st);
         case 4: return run_tail_tc_ke<D, 4, true>(KE, G, grid, smem, scratch_bytes, st);
         case 8: return run_tail_tc_ke<D, 8, true>(KE, G, grid, smem, scratch_bytes, st);
+        case 16: return run_tail_tc_ke<D, 16, true>(KE, G, grid, smem, scratch_bytes, st);
         default: return cudaErrorInvalidValue;
       }
     }
@@ -226,6 +229,7 @@ cudaError_t Launcher<BF16, D>::tail_tc(int NC, int KE, bool group, const Geom& G
       case 2: return run_tail_tc_ke<D, 2, false>(KE, G, grid, smem, scratch_bytes, st);
       case 4: return run_tail_tc_ke<D, 4, false>(KE, G, grid, smem, scratch_bytes, st);
       case 8: return run_tail_tc_ke<D, 8, false>(KE, G, grid, smem, scratch_bytes, st);
+      case 16: return run_tail_tc_ke<D, 16, false>(KE, G, grid, smem, scratch_bytes, st);
       default: return cudaErrorInvalidValue;
     }
   }

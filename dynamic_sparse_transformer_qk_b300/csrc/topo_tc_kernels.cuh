@@ -250,7 +250,8 @@ __device__ __forceinline__ TcSplits tc_splits(const Geom& G, int b, int kvh, lon
 //
 // Grid and workspace as topo_select_kernel (grid.x = column block x split,
 // grid.y = KV head, grid.z = sequence); a split is G.L keys (a multiple of
-// 128).  bf16 only; k <= 32 * KE, KE <= 2; NC <= 8 / KE columns per block.
+// 128).  bf16 only; k <= 32 * KE, KE <= 2; NC <= 16 columns per block (the
+// MMA's N) with KE = 1, NC <= 4 with KE = 2.
 //
 // GROUP: group-shared selection (grouped-query attention).  The block's
 // columns are (row, head) pairs, col = row * g + head; the g heads of a row
@@ -272,7 +273,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int TILEB = kTcTile * S::ROWB;
   constexpr int KSTEPS = D / 16;      // MMA K = 16 bf16 per instruction
   constexpr int NL = NC <= 4 ? 4 : (NC <= 8 ? 8 : 16);
-  static_assert(NC <= 8 / KE && KE <= 2 && LL + 32 <= CAP && cap_for(KE) <= CAP,
+  static_assert((KE == 1 ? NC <= kTcN : NC <= 4) && KE <= 2 && LL + 32 <= CAP &&
+                    cap_for(KE) <= CAP,
                 "tensor-core select shape");
 
   const int b = blockIdx.z, kvh = blockIdx.y;
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float coef[NC], T[NC], thr[NC];
     int cnt[NC];
     bool ovf[NC];
-    long long jh[NC];
+    int jh[NC];  // last candidate position per column (< 2^31)
     const int gsz = GROUP ? G.g : 1;  // heads per selection column
 #pragma unroll
     for (int h = 0; h < NC; ++h) {
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       thr[h] = -INFINITY;
       cnt[h] = 0;
       ovf[h] = false;
-      jh[h] = cols[h].active ? (cols[h].jhi < ke ? cols[h].jhi : ke) : 0;
+      jh[h] = cols[h].active ? (int)(cols[h].jhi < ke ? cols[h].jhi : ke) : 0;
     }
     if constexpr (GROUP) {
       // selection column s covers columns s*g .. s*g+g-1: the largest
@@ -670,8 +672,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else {
+    // one warp per column, each warp reusing its own area of the ring
     for (int h = ew; h >= 0 && h < nsel; h += kTcEpiWarps) {
-      uint64_t* cat = reinterpret_cast<uint64_t*>(ring) + (size_t)h * kTcEpiWarps * CAP;
+      uint64_t* cat = reinterpret_cast<uint64_t*>(ring) + (size_t)ew * kTcEpiWarps * CAP;
       int ns = 0;
       const int ov = gather(h, cat, ns);
       uint64_t x[LE];

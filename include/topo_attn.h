@@ -138,7 +138,7 @@ int topo_attn_forward(const topo_attn_params *p, const void *q, const void *k, c
  *   out : required, [B, Hq, nq, d] float32.
  *   idx : optional, [B, Hkv, nq, 1+W+k] int32 (one row per group).
  * Workspace: topo_attn_workspace_size(p).  Supported: bf16, Hq/Hkv >= 2,
- * nq * Hq/Hkv <= 8 (<= 4 when k > 32), 1 <= k <= 64 (the tensor-core decode
+ * nq * Hq/Hkv <= 16 (<= 4 when k > 32), 1 <= k <= 64 (the tensor-core decode
  * shapes); otherwise TOPO_ERR_UNSUPPORTED.
  */
 int topo_attn_forward_grouped(const topo_attn_params *p, const void *q, const void *k,
@@ -180,7 +180,7 @@ size_t topo_attn_paged_workspace_size(const topo_attn_params *p, const topo_page
  * over a paged or contiguous KV cache with per-sequence lengths and a float32
  * or bfloat16 output.  p->n is the largest sequence length (p->kv_stride is
  * read only for a contiguous cache).  Supported on the tensor-core decode
- * shapes: bf16, nq * Hq/Hkv <= 8 (<= 4 when k > 32), 1 <= k <= 64; otherwise
+ * shapes: bf16, nq * Hq/Hkv <= 16 (<= 4 when k > 32), 1 <= k <= 64; otherwise
  * TOPO_ERR_UNSUPPORTED.  idx (optional) as for topo_attn_forward.
  */
 int topo_attn_forward_paged(const topo_attn_params *p, const topo_paged_kv *kv, const void *q,

@@ -47,6 +47,9 @@ SHAPES = [
                       planted=32)),
     ("short", dict(Hq=8, Hkv=2, n=150, nq=1, W=10, k=32)),
     ("wide_window", dict(d=64, Hq=4, Hkv=1, n=6000, nq=1, W=5000, k=32)),
+    # 16 query heads per KV head: 16 tensor-core columns per block
+    ("g16", dict(Hq=64, Hkv=4, n=15000, nq=1, W=64, k=32, planted=16)),
+    ("g8_nq2", dict(d=64, Hq=16, Hkv=2, n=8000, nq=2, W=40, k=20)),
 ]
 
 

@@ -38,6 +38,18 @@ def test_decode_32k_bf16():
     _full(synth.CONFIGS[1])
 
 
+@pytest.mark.parametrize("kw", [
+    dict(Hq=64, Hkv=4, n=20000, planted=16),             # 16:1 GQA decode
+    dict(Hq=32, Hkv=4, n=9000, nq=2, W=32, k=24),         # 8 heads x 2 rows
+    dict(Hq=16, Hkv=4, n=5000, nq=3, W=48, k=32),         # 12 of 16 columns
+    dict(d=64, Hq=32, Hkv=2, n=7000, nq=1, k=7, W=9),     # d = 64
+], ids=["g16", "g8_nq2", "g4_nq3", "g16_d64"])
+def test_decode_sixteen_columns_per_kv_head(kw):
+    """Up to 16 query columns per KV head on the tensor-core decode scorer
+    (the MMA's N): every row against the oracle, excluded mass included."""
+    _full(synth.CONFIGS[1].with_(**kw))
+
+
 def test_decode_32k_planted_keys_found():
     w = synth.CONFIGS[1]
     x = synth.make(w)
