@@ -344,12 +344,14 @@ def measure_decode(args, w: synth.Workload, dev, rank: int, world: int, local: i
                 "kernel": "topo_select_tc_kernel",
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "timing": "CUDA events around each replay of the captured step "
-                          "(one counter memset + one kernel)",
+                          "(counter memset, select kernel, dependent tail kernel)",
                 "traffic": traffic_from_profile("topo_select_tc_kernel",
                                                 "decode-1m" if w.n == 1048576 and w.B == 1
                                                 else "none")}
     rec = {"ms_per_step": ms, "value": value, "unit": "queries/s", "roofline": roofline,
-           "clocks": clk.summary(), "queries_per_step": queries, "gpu_launches": steps,
+           "clocks": clk.summary(), "queries_per_step": queries,
+           # per step: the select kernel and its dependent tail kernel
+           "gpu_launches": 2 * steps,
            "config": {"workload": workload_desc(w),
                       "l2": (f"K cache {k_bytes / 1e9:.3f} GB < 2x L2: 256 MB write between "
                              "timed steps" if l2_flush else
@@ -490,11 +492,13 @@ def measure_layers(args, dev, local: int, *, steps: int, L: int = 32, n: int = 1
                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                         "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
                         "algorithmic_bytes_per_step": alg,
-                        "kernel": "topo_select_tc_kernel (sparse layers) + dense_kernel (pillars)",
+                        "kernel": "topo_select_tc_kernel (sparse layers) + dense_tc_kernel (pillars)",
                         "timing": f"CUDA events around each replay of the captured {L}-layer step",
                         "traffic": None},
            "all_dense_ms_per_step": dense_ms, "pillar_speedup_vs_all_dense": dense_ms / ms,
-           "clocks": clk.summary(), "gpu_launches": 2 * L * steps,
+           "clocks": clk.summary(),
+           # per step: select + tail kernels per sparse layer, one dense kernel per pillar
+           "gpu_launches": sum(1 if s["dense"] else 2 for s in sch) * steps,
            "config": {"workload": f"{L} layers x (decode n={n}, 32/8 heads, d=128, bf16); "
                                   "pillars (dense) at layers 0 and 16; W 256/128/64 by depth "
                                   "third; k=32; every layer its own seeded q, K, V",
