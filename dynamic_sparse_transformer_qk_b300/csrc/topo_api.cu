@@ -520,6 +520,9 @@ int run_topo(const topo_attn_params* p, const void* q, const void* k, const void
         topo::TailSmem(tail_scratch, P.D, P.NC, P.KP).total;
     const bool split_tail = tail_smem <= topo::kMaxSmem;
     if (split_tail) G.flags |= topo::kSplitTail;
+    // one wave of select CTAs: the tail's band staging may overlap its end
+    if (split_tail && (P.hi_units > 0 || P.units * P.nsplit <= sm_count()))
+      G.flags |= topo::kEarlyBand;
     rc = dispatch(P.bf16, P.D, [&](auto L) {
       return L.select_tc(P.NC, P.KE, group, mk128, G, grid, P.smem, st);
     });

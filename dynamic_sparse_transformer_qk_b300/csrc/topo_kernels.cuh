@@ -31,7 +31,10 @@ namespace topo {
 
 // kSplitTail: the tensor-core select kernel only publishes its split lists;
 // a dependent tail kernel merges them (one CTA per selection column).
-enum : int { kDoIdx = 1, kDoPV = 2, kSaveThr = 4, kSplitTail = 8 };
+// kEarlyBand: the tail kernel stages the window band before waiting for the
+// select grid (measured to help when the select grid is one wave, and to cost
+// ~25 us at B = 16 x 128K with seven waves).
+enum : int { kDoIdx = 1, kDoPV = 2, kSaveThr = 4, kSplitTail = 8, kEarlyBand = 16 };
 
 // Everything a kernel needs, passed by value.
 struct Geom {
@@ -583,7 +586,7 @@ template <bool BF16, int D, int NC, int KE, int NW, bool GROUP = false>
 __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nsplit, int b, int kvh,
                                          const ColInfo* cols, const float2* qd, uint64_t* run,
                                          uint8_t* scratch, int scratch_bytes, int h0 = 0,
-                                         int h1 = NC) {
+                                         int h1 = NC, int part = 0) {
   using S = Shape<BF16, D>;
   constexpr int KP = 32 * KE;
   // a staged slot: the K row, then the V row, then 16 bytes of padding, so
@@ -630,21 +633,22 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
   const uint8_t* vb = reinterpret_cast<const uint8_t*>(G.vp);
 
   for (int i = tid; i < NC * KP; i += blockDim.x) run[i] = 0ull;
-  if (fast) {
+  // One selection column (the tail kernel's CTAs): every warp merges a
+  // strided subset of the splits' lists of that column, read from L2, and
+  // warp 0 merges the warps' results (NW partial lists in the list area).
+  const bool one_sel = (GROUP ? h1 - h0 == G.g : h1 - h0 == 1) &&
+                       (long long)nsplit * NC >= NW;
+  // part 1 issues the band and anchor rows only (they do not depend on the
+  // selection: the tail kernel starts them before waiting for the lists);
+  // part 2 is the rest; part 0 both.
+  if (fast && part != 2) {
     if (tid == 0) {
       for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
       fence_mbar_init();
     }
-    // the split lists were written by other CTAs through the generic proxy
-    asm volatile("fence.proxy.async;" ::: "memory");
     __syncthreads();
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&bars[0], (uint32_t)list_bytes);
-      bulk_copy_g2s(scratch + v0, G.lists + (size_t)unit * G.nsplit_max * per_split,
-                    (uint32_t)list_bytes, &bars[0]);
+    if (tid == 0)
       mbar_arrive_expect_tx(&bars[1], (uint32_t)((nb + (band_lo == 0 ? 0 : 1)) * 2 * S::ROWB));
-    }
-    // band and anchor rows are known already: start them now
     for (long long sl = tid; sl < top0; sl += blockDim.x) {
       long long row = sl < nb ? band_lo + sl : (band_lo == 0 ? -1 : 0);
       if (row < 0) continue;
@@ -653,8 +657,48 @@ __device__ __noinline__ void select_tail(const Geom& G, long long unit, int nspl
       bulk_copy_g2s(dst, kb + gr * S::ROWB, S::ROWB, &bars[1]);
       bulk_copy_g2s(dst + S::ROWB, vb + gr * S::ROWB, S::ROWB, &bars[1]);
     }
-    if (!mbar_wait(&bars[0], 0) && tid == 0) set_status(G.status, kStatusTimeout);
-    for (int h = warp; h < nsel; h += NW) {
+  }
+  if (part == 1) return;
+  if (fast) {
+    // the split lists were written by other CTAs through the generic proxy
+    asm volatile("fence.proxy.async;" ::: "memory");
+    __syncthreads();
+    if (tid == 0 && !one_sel) {
+      mbar_arrive_expect_tx(&bars[0], (uint32_t)list_bytes);
+      bulk_copy_g2s(scratch + v0, G.lists + (size_t)unit * G.nsplit_max * per_split,
+                    (uint32_t)list_bytes, &bars[0]);
+    }
+    if (one_sel) {
+      const int hs = GROUP ? h0 / G.g : h0;
+      uint64_t a[KE];
+#pragma unroll
+      for (int e = 0; e < KE; ++e) a[e] = 0ull;
+      for (int s2 = warp; s2 < nsplit; s2 += NW) {
+        const unsigned long long* src =
+            G.lists + ((size_t)unit * G.nsplit_max + s2) * per_split + (size_t)hs * KP;
+        uint64_t bb[KE];
+#pragma unroll
+        for (int e = 0; e < KE; ++e) bb[e] = __ldcg(src + e * 32 + lane);
+        warp_merge_desc<KE>(a, bb, lane);
+      }
+      uint64_t* part = reinterpret_cast<uint64_t*>(scratch + v0);  // [NW][KP]
+#pragma unroll
+      for (int e = 0; e < KE; ++e) part[warp * KP + e * 32 + lane] = a[e];
+      __syncthreads();
+      if (warp == 0) {
+        for (int w = 1; w < NW; ++w) {
+          uint64_t bb[KE];
+#pragma unroll
+          for (int e = 0; e < KE; ++e) bb[e] = part[w * KP + e * 32 + lane];
+          warp_merge_desc<KE>(a, bb, lane);
+        }
+#pragma unroll
+        for (int e = 0; e < KE; ++e) run[hs * KP + e * 32 + lane] = a[e];
+      }
+      __syncthreads();
+    }
+    if (!one_sel && !mbar_wait(&bars[0], 0) && tid == 0) set_status(G.status, kStatusTimeout);
+    for (int h = warp; h < nsel && !one_sel; h += NW) {
       if (!cols[GROUP ? h * G.g : h].active) continue;
       const uint64_t* lb = reinterpret_cast<const uint64_t*>(scratch + v0);
       uint64_t a[KE];

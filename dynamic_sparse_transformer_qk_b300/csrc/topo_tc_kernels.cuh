@@ -710,8 +710,9 @@ struct TailSmem {
   }
 };
 
+// Two CTAs per SM (registers <= 102): batched decode runs hundreds of tails.
 template <int D, int NC, int KE, bool GROUP>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     topo_tail_tc_kernel(const Geom G, int scratch_bytes) {
   constexpr int KP = 32 * KE;
   const int b = blockIdx.z, kvh = blockIdx.y;
@@ -727,11 +728,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x < NC && ((int)threadIdx.x < h0 || (int)threadIdx.x >= h1))
     cols[threadIdx.x].active = 0;
   const TcSplits sp = tc_splits(G, b, kvh, 0);
+  // the window band and anchor rows do not depend on the selection: with
+  // kEarlyBand, start staging them before waiting
+  const bool early = (G.flags & kEarlyBand) != 0;
+  if (early)
+    select_tail<true, D, NC, KE, kTcWarps, GROUP>(G, sp.unit, sp.nsplit, b, kvh, cols, qd, run,
+                                                  sm, scratch_bytes, h0, h1, 1);
   // the select grid has completed and its lists are visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   select_tail<true, D, NC, KE, kTcWarps, GROUP>(G, sp.unit, sp.nsplit, b, kvh, cols, qd, run, sm,
-                                                scratch_bytes, h0, h1);
+                                                scratch_bytes, h0, h1, early ? 2 : 0);
 }
 
 // ============================================ tensor-core dense attention ====
