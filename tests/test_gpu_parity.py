@@ -133,6 +133,10 @@ TC_DECODE = [
     ("nan_tail", dict(d=128, Hq=8, Hkv=2, n=10000, nq=1, kv_stride=10300, nan_tail=True,
                       W=64, k=32, planted=32)),
     ("wide_window", dict(d=64, Hq=4, Hkv=1, n=6000, nq=1, W=5000, k=32)),
+    # the dependent tail kernel's staged softmax fits one CTA at W = 256 and
+    # not at W = 400 (the select kernel's own tail takes over)
+    ("w256_split_tail", dict(d=128, Hq=32, Hkv=8, n=30000, nq=1, W=256, k=32, planted=32)),
+    ("w400_in_kernel_tail", dict(d=128, Hq=8, Hkv=2, n=20000, nq=1, W=400, k=32, planted=8)),
 ]
 
 
