@@ -972,39 +972,50 @@ __global__ void __launch_bounds__(kPbWarps * 32, 1) prefill_pv_band_kernel(const
     float mx[kPbUnit];
 #pragma unroll
     for (int r = 0; r < kPbUnit; ++r) mx[r] = -INFINITY;
-    // two keys per lane at a time (e and e + 32): eight independent chains,
-    // every query load serves both
+    // two keys per lane at a time (e and e + 32), every query load serving
+    // both; the dot products run as paired FMAs over (even, odd) elements
+    // (softmax logits only: the selection is already made, so the two halves
+    // may be added at the end)
     for (int e0 = 0; e0 < nw; e0 += 64) {
       const int ea = e0 + lane, eb = e0 + 32 + lane;
       const bool va = ea < nw, vbk = eb < nw;
       const uint4* kra = reinterpret_cast<const uint4*>(kb + (size_t)(jlo + (va ? ea : 0) - band_lo) * ROWP);
       const uint4* krb = reinterpret_cast<const uint4*>(kb + (size_t)(jlo + (vbk ? eb : 0) - band_lo) * ROWP);
-      float aa[kPbUnit], ab[kPbUnit];
+      float2 a2[kPbUnit], b2[kPbUnit];
 #pragma unroll
       for (int r = 0; r < kPbUnit; ++r) {
-        aa[r] = 0.f;
-        ab[r] = 0.f;
+        a2[r] = make_float2(0.f, 0.f);
+        b2[r] = make_float2(0.f, 0.f);
       }
 #pragma unroll 2
       for (int v = 0; v < S::ROWB / 16; ++v) {
         const uint4 wa4 = kra[v], wb4 = krb[v];
-        float xa[8], xb[8];
+        const uint32_t ua[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
+        const uint32_t ub[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
+        float2 xa[4], xb[4];  // elements (2i, 2i+1) of the two rows
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          xa[x] = chunk_elem<true>(wa4, x);
-          xb[x] = chunk_elem<true>(wb4, x);
+        for (int i = 0; i < 4; ++i) {
+          xa[i] = make_float2(__uint_as_float(ua[i] << 16), __uint_as_float(ua[i] & 0xffff0000u));
+          xb[i] = make_float2(__uint_as_float(ub[i] << 16), __uint_as_float(ub[i] & 0xffff0000u));
         }
 #pragma unroll
         for (int r = 0; r < kPbUnit; ++r) {
           const float4* q4 = reinterpret_cast<const float4*>(qw + r * D + v * 8);
           const float4 qa = q4[0], qb = q4[1];
-          const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+          const float2 qp[4] = {make_float2(qa.x, qa.y), make_float2(qa.z, qa.w),
+                                make_float2(qb.x, qb.y), make_float2(qb.z, qb.w)};
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            aa[r] = fmaf(qq[x], xa[x], aa[r]);
-            ab[r] = fmaf(qq[x], xb[x], ab[r]);
+          for (int i = 0; i < 4; ++i) {
+            a2[r] = __ffma2_rn(qp[i], xa[i], a2[r]);
+            b2[r] = __ffma2_rn(qp[i], xb[i], b2[r]);
           }
         }
+      }
+      float aa[kPbUnit], ab[kPbUnit];
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r) {
+        aa[r] = a2[r].x + a2[r].y;
+        ab[r] = b2[r].x + b2[r].y;
       }
 #pragma unroll
       for (int r = 0; r < kPbUnit; ++r) {
@@ -1074,16 +1085,33 @@ __global__ void __launch_bounds__(kPbWarps * 32, 1) prefill_pv_band_kernel(const
         for (int x = 0; x < EPL; ++x) acc[r][x] = w0 * va[x];
       }
     }
+    {
+      static_assert(EPL % 2 == 0, "element pairs per lane");
+      float2 acc2[kPbUnit][EPL / 2];
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r)
+#pragma unroll
+        for (int x = 0; x < EPL / 2; ++x) acc2[r][x] = make_float2(acc[r][2 * x], acc[r][2 * x + 1]);
 #pragma unroll 2
-    for (int e = 0; e < nw; ++e) {
-      float vv[EPL];
-      lane_elems<true, D>(vb + (size_t)(jlo + e - band_lo) * ROWP + lane * S::BPL, vv);
+      for (int e = 0; e < nw; ++e) {
+        float vv[EPL];
+        lane_elems<true, D>(vb + (size_t)(jlo + e - band_lo) * ROWP + lane * S::BPL, vv);
 #pragma unroll
-      for (int r = 0; r < kPbUnit; ++r) {
-        const float w = lw[r * wbp + e];
+        for (int r = 0; r < kPbUnit; ++r) {
+          const float w = lw[r * wbp + e];
 #pragma unroll
-        for (int x = 0; x < EPL; ++x) acc[r][x] = fmaf(w, vv[x], acc[r][x]);
+          for (int x = 0; x < EPL / 2; ++x)
+            acc2[r][x] = __ffma2_rn(make_float2(w, w), make_float2(vv[2 * x], vv[2 * x + 1]),
+                                    acc2[r][x]);
+        }
       }
+#pragma unroll
+      for (int r = 0; r < kPbUnit; ++r)
+#pragma unroll
+        for (int x = 0; x < EPL / 2; ++x) {
+          acc[r][2 * x] = acc2[r][x].x;
+          acc[r][2 * x + 1] = acc2[r][x].y;
+        }
     }
 #pragma unroll
     for (int r = 0; r < kPbUnit; ++r) {
