@@ -564,19 +564,23 @@ __device__ __forceinline__ void warp_softmax_pv(const Geom& G, int b, int kvh, c
 }
 
 // Tail of the select kernels, run by the CTA that finished a column block
-// last: merge the splits' exact top-k lists, then per column write C_i, the
-// k-th key (for the excluded-mass pass) and the softmax over C_i.  `run` holds
-// NC * KP keys; `scratch` (1024-byte aligned, at least NC*KP*4 + NC*8 + 1024
-// + NW*2048 bytes and one split's lists) is free shared memory.
+// last, or by a CTA of the dependent tail kernel for the columns h0..h1-1
+// (the others inactive): merge the splits' exact top-k lists, then per column
+// write C_i, the k-th key (for the excluded-mass pass) and the softmax over
+// C_i.  `run` holds NC * KP keys; `scratch` (1024-byte aligned, at least
+// NC*KP*4 + NC*8 + 1024 + NW*2048 bytes and one split's lists) is free shared
+// memory.
 //
-// Fast path, when everything fits in `scratch`: the lists of all splits come
-// in with one bulk copy; the rows every softmax needs (the band covering the
-// block's windows and the anchor, then each column's top-k) are staged with
-// bulk copies, the band ones issued before the merge; logits are computed by
-// all threads, then one thread per (column, output element) forms the
-// weighted sum of V.  Otherwise the lists are read in chunks and one warp per
-// column reads its rows from global memory.  All threads of the CTA call this;
-// warps 0..NW-1 do the per-column work.
+// Fast path, when everything fits in `scratch`: the rows every softmax needs
+// (the band covering the block's windows and the anchor, then each column's
+// top-k) are staged with bulk copies, the band ones first (part 1 issues only
+// those, part 2 does the rest, part 0 both); the lists of all splits come in
+// with one bulk copy, or, for a single selection column, every warp merges a
+// strided subset of its lists from L2 and warp 0 the warps' results; logits
+// are computed by all threads, then one thread per (column, output element)
+// forms the weighted sum of V.  Otherwise the lists are read in chunks and one
+// warp per column reads its rows from global memory.  All threads of the CTA
+// call this; warps 0..NW-1 do the per-column work.
 //
 // GROUP: the lists are per selection column s (one per row of the block, for
 // the g heads col = s*g .. s*g+g-1, see topo_select_tc_kernel); after the

@@ -30,8 +30,9 @@
 //                            (delta: the bound on |tensor core - exact chain|,
 //                            see topo_tc_kernels.cuh).  Pass 2 appends every
 //                            score above the cut and, when a buffer fills,
-//                            the warp compacts that column (a bisection on
-//                            warp-wide counts), raising the cut.  Survivors,
+//                            compacts that column (its owner thread bisects
+//                            over the buffered scores in registers), raising
+//                            the cut.  Survivors,
 //                            with their tensor-core scores, go to the
 //                            workspace;
 //   prefill_finalize_kernel  one warp per column: the exact top-k (ties to the
@@ -43,8 +44,13 @@
 //                            requested, the exact k-th key.  A column whose
 //                            near ties overflowed its buffer is rescanned
 //                            exactly on CUDA cores;
-//   prefill_pv_kernel        one warp per row: float32 online softmax over
-//                            C_i and the weighted sum of V.
+//   prefill_pv_band_kernel   32 consecutive rows of one head share their
+//                            window band, staged once in shared memory; per
+//                            row the float32 softmax over C_i (band, anchor,
+//                            and the top-k with the finalize kernel's exact
+//                            logits) and the weighted sum of V;
+//   prefill_pv_kernel        the same with one warp per row and rows read from
+//                            global memory, when the band does not fit.
 #pragma once
 
 #include <cuda_bf16.h>
